@@ -1,0 +1,762 @@
+"""Benchmark of the GB300 KV-cache write path.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one pass of the write path over one batch of synthetic input.  The
+default workload is the fused K RMSNorm + RoPE + V41 store of 16384 bf16 rows
+into a 2^20-slot paged pool (the largest batch of the store sweep); other
+workloads (--workload) cover the FP4 store, the full-pool dequant, the
+translated C4A compressor and the mixed C128A compressor.
+
+The timed region replays CUDA graphs holding exactly K steps (captured
+launches of the C ABI), bracketed by a barrier and a synchronize, timed with
+CUDA events on the launching stream; inputs rotate over enough distinct sets
+that every step reads from HBM (the rotation set exceeds the 129 MB L2).
+Rank 0 prints one JSON line.  --impl reference times the CPU oracle on a
+bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+L2_BYTES = 129 * 2**20
+FALLBACK_HBM_GBS = 6800.0
+METRIC = "KV tokens/s and achieved HBM GB/s (% of GB300 roofline) per layout/ratio"
+
+# algorithmic bytes per unit (rows read + loc + pos + cos/sin row + payload written)
+B_STORE = 1024 + 8 + 528
+B_STORE_ROPE = B_STORE + 4 + 256
+B_FP4_STORE = 1024 + 8 + 272
+B_FP4_DEQ = 272 + 1024
+B_TRANSLATE = 8 + 4 + 4
+
+
+def b_compress(r, payload=528):
+    return r * 4096 + 4 + 4 + 256 + payload
+
+
+DEFAULT_STEPS = {
+    "store_norm_rope": 200000, "store_rope": 200000, "store": 200000, "small": 200000,
+    "fp4_store": 20000, "fp4_dequant": 3000, "c4a": 20000, "c128a": 1000, "c128a_fp4": 1000,
+}
+
+# the workloads: one per configuration of the write path
+SPECS = {
+    "small": dict(kind="store", flags=0, bs=64, pool_slots=256, layout=1, fp32=True),
+    "store": dict(kind="store", flags=0, bs=16384, pool_slots=1 << 20, layout=1),
+    "store_rope": dict(kind="store", flags=1, bs=16384, pool_slots=1 << 20, layout=1),
+    "store_norm_rope": dict(kind="store", flags=3, bs=16384, pool_slots=1 << 20, layout=1),
+    "fp4_store": dict(kind="store", flags=0, bs=262144, pool_slots=1 << 21, layout=2, student_t=True),
+    "fp4_dequant": dict(kind="dequant", pool_slots=1 << 21, layout=2),
+    "c4a": dict(kind="compress", ratio=4, layout=1, score_std=math.sqrt(2.0), groups=16384,
+                full_slots=1 << 20, swa_slots=1 << 17),
+    "c128a": dict(kind="compress", ratio=128, layout=1, score_std=2.0, requests=256,
+                  pool_slots=1 << 20),
+    "c128a_fp4": dict(kind="compress", ratio=128, layout=2, score_std=2.0, requests=256,
+                      pool_slots=1 << 20),
+}
+
+
+def describe(name):
+    """(config dict, unit name) of a workload, without touching a GPU."""
+    sp = SPECS[name]
+    lay = "V41" if sp["layout"] == 1 else "V41_FP4"
+    if sp["kind"] == "store":
+        cfg = {"workload": name, "layout": lay, "flags": {0: "none", 1: "rope", 3: "norm+rope"}[sp["flags"]],
+               "bs": sp["bs"], "x_dtype": "f32" if sp.get("fp32") else "bf16", "loc_dtype": "int64",
+               "page_size": 64, "pool_slots": sp["pool_slots"],
+               "rows": "0.5*Student-t(3)" if sp.get("student_t") else
+                       ("N(0,1)" if sp.get("fp32") else "N(0,1), 1% x50 outliers")}
+        if sp["flags"] & 1:
+            cfg["rope"] = "last 64 dims, theta 1e4, positions U[0,65536), fp32 table"
+        if sp["flags"] & 2:
+            cfg["norm"] = "RMSNorm over 512 dims, w~N(1,0.1), eps 1e-6"
+        return cfg, "tokens"
+    if sp["kind"] == "dequant":
+        return {"workload": name, "layout": lay, "tokens": sp["pool_slots"], "page_size": 64,
+                "page_table": "random permutation of the pool's pages",
+                "rows": "0.5*Student-t(3) stored by the FP4 store"}, "tokens"
+    cfg = {"workload": name, "layout": lay, "ratio": sp["ratio"], "page_size": 64,
+           "values": "N(0,1) fp32", "scores": f"N(0,{sp['score_std'] ** 2:g}) fp32",
+           "rope": "last 64 dims at the group's position"}
+    if sp["ratio"] == 4:
+        cfg.update(groups=sp["groups"], input_tokens=sp["groups"] * 4, full_slots=sp["full_slots"],
+                   swa_slots=sp["swa_slots"], translate="once per step, int64 full loc -> int32 SWA slot")
+    else:
+        cfg.update(requests=sp["requests"], lengths="log-uniform [128, 32768], multiples of 128",
+                   pool_slots=sp["pool_slots"])
+    return cfg, "input tokens"
+
+
+# ----------------------------------------------------------------------------- workloads
+
+class Workload:
+    """Inputs on the GPU, one step, and the numbers that describe it."""
+
+    R = 1                     # rotating input sets
+    units = 0                 # KV tokens per step (the metric's unit)
+    bytes_total = 0           # algorithmic bytes per step, all kernels
+    bytes_dominant = 0        # algorithmic bytes of the dominant kernel per launch
+    launches = 1              # our kernel launches per step
+    dominant = ""
+
+    def __init__(self, name, dev):
+        import compress_kv_write_gb300 as K
+        import torch
+        self.K, self.name, self.dev = K, name, dev
+        self.spec = SPECS[name]
+        self.config, self.unit_name = describe(name)
+        self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def step(self, i):
+        raise NotImplementedError
+
+    def dominant_step(self, i):
+        self.step(i)
+
+
+def _rotation(per_set_bytes, cap=64):
+    return max(1, min(cap, math.ceil(2.5 * L2_BYTES / max(1, per_set_bytes))))
+
+
+class StoreWorkload(Workload):
+    """bs rows -> paged pool: store, store + RoPE, fused K RMSNorm + RoPE."""
+
+    def __init__(self, name, dev):
+        super().__init__(name, dev)
+        import torch
+        from compress_kv_write_gb300 import synth
+        sp = self.spec
+        self.flags, self.bs, self.layout = sp["flags"], sp["bs"], sp["layout"]
+        self.pool_slots = sp["pool_slots"]
+        bs = self.bs
+        self.pool = torch.zeros(self.pool_slots * self.K.bytes_per_token(self.layout),
+                                dtype=torch.uint8, device=dev)
+        row_bytes = 2048 if sp.get("fp32") else 1024
+        self.R = _rotation(bs * (row_bytes + 12))
+        self.x, self.loc, self.pos = [], [], []
+        for r in range(self.R):
+            if sp.get("fp32"):
+                x = synth.normal((bs, 512), dev, r, "x")
+            elif sp.get("student_t"):
+                x = synth.student_t_rows_bf16(bs, dev, r)
+            else:
+                x = synth.store_rows_bf16(bs, dev, r)
+            self.x.append(x)
+            self.loc.append(synth.injective_slots(bs, self.pool_slots, dev, r))
+            self.pos.append(synth.positions(bs, dev, r))
+        self.cs = synth.rope_table(65536, dev)
+        self.w = synth.norm_weight(dev, 0)
+        self.units = bs
+        payload = 528 if self.layout == 1 else 272
+        per = row_bytes + 8 + payload + ((4 + 256) if self.flags & 1 else 0)
+        self.bytes_total = self.bytes_dominant = bs * per
+        self.dominant = "store_kernel"
+        total = self.R * bs * (row_bytes + 12)
+        self.config["l2"] = (f"rotating {self.R} input sets ({total / 2**20:.0f} MB > 129 MB L2)"
+                             if total > L2_BYTES else
+                             f"latency config: {self.R} input sets ({total / 2**20:.1f} MB) stay in L2")
+
+    def _store(self, x, loc, pos):
+        rope = self.flags & 1
+        self.K.kvq_store(self.layout, 6, self.flags, x, loc, self.pool, self.pool_slots,
+                         norm_weight=self.w if self.flags & 2 else None, eps=1e-6,
+                         cos_sin=self.cs if rope else None, pos=pos if rope else None, err=self.err)
+
+    def step(self, i):
+        r = i % self.R
+        self._store(self.x[r], self.loc[r], self.pos[r])
+
+    # end to end: the step's rows, slots and positions come from pinned host memory
+    def e2e_setup(self):
+        import torch
+        self.hx = self.x[0].cpu().pin_memory()
+        self.hloc = self.loc[0].cpu().pin_memory()
+        self.hpos = self.pos[0].cpu().pin_memory()
+        self.dx = torch.empty_like(self.x[0])
+        self.dloc = torch.empty_like(self.loc[0])
+        self.dpos = torch.empty_like(self.pos[0])
+        self.herr = torch.zeros(1, dtype=torch.int32).pin_memory()
+        h2d = self.hx.numel() * self.hx.element_size() + self.hloc.numel() * 8
+        if self.flags & 1:
+            h2d += self.hpos.numel() * 4
+        return h2d, 4
+
+    def e2e_step(self):
+        self.dx.copy_(self.hx, non_blocking=True)
+        self.dloc.copy_(self.hloc, non_blocking=True)
+        if self.flags & 1:
+            self.dpos.copy_(self.hpos, non_blocking=True)
+        self._store(self.dx, self.dloc, self.dpos)
+        self.herr.copy_(self.err, non_blocking=True)
+
+
+class DequantWorkload(Workload):
+    """Full-pool paged dequant of a 2^21-slot FP4 pool into a bf16 workspace."""
+
+    def __init__(self, name, dev):
+        super().__init__(name, dev)
+        import torch
+        from compress_kv_write_gb300 import synth
+        self.layout, self.pool_slots = self.spec["layout"], self.spec["pool_slots"]
+        self.pool = torch.zeros(self.pool_slots * self.K.bytes_per_token(self.layout),
+                                dtype=torch.uint8, device=dev)
+        chunk = 1 << 18
+        x = synth.student_t_rows_bf16(chunk, dev, 0)
+        for c in range(self.pool_slots // chunk):     # fill the pool with the FP4 store
+            loc = torch.arange(c * chunk, (c + 1) * chunk, device=dev)
+            self.K.kvq_store(self.layout, 6, 0, x, loc, self.pool, self.pool_slots)
+        del x
+        self.n_pages = self.pool_slots >> 6
+        self.pt = synth.page_table_perm(self.n_pages, dev, 0)
+        self.out = torch.empty((self.pool_slots, 512), dtype=torch.bfloat16, device=dev)
+        self.units = self.pool_slots
+        self.bytes_total = self.bytes_dominant = self.pool_slots * B_FP4_DEQ + self.n_pages * 4
+        self.dominant = "dequant_kernel"
+        self.config["l2"] = (f"pool {self.pool_slots * 288 / 2**20:.0f} MB read + workspace "
+                             f"{self.pool_slots * 1024 / 2**20:.0f} MB written per step > 129 MB L2")
+
+    def step(self, i):
+        self.K.kvq_dequant(self.layout, 6, self.pool, self.n_pages, self.pt, self.out, err=self.err)
+
+    def e2e_setup(self):
+        import torch
+        self.hpt = self.pt.cpu().pin_memory()
+        self.dpt = torch.empty_like(self.pt)
+        self.hout = torch.empty((self.pool_slots, 512), dtype=torch.bfloat16).pin_memory()
+        return self.hpt.numel() * 4, self.hout.numel() * 2
+
+    def e2e_step(self):
+        self.dpt.copy_(self.hpt, non_blocking=True)
+        self.K.kvq_dequant(self.layout, 6, self.pool, self.n_pages, self.dpt, self.out, err=self.err)
+        self.hout.copy_(self.out, non_blocking=True)
+
+
+class CompressWorkload(Workload):
+    """Ratio-r softmax compressor; C4A also translates its slots once per step."""
+
+    def __init__(self, name, dev):
+        super().__init__(name, dev)
+        import torch
+        from compress_kv_write_gb300 import synth
+        sp = self.spec
+        self.r, self.layout = sp["ratio"], sp["layout"]
+        payload = 528 if self.layout == 1 else 272
+        r = self.r
+        if r == 4:
+            G = sp["groups"]
+            self.full_slots, self.pool_slots = sp["full_slots"], sp["swa_slots"]
+            per_set = G * r * 4096
+            self.R = _rotation(per_set, cap=8)
+            self.v, self.s, self.full_loc, self.table = [], [], [], []
+            for k in range(self.R):
+                v, s = synth.compressor_rows(G * r, dev, k, score_std=sp["score_std"])
+                fl = synth.injective_slots(G, self.full_slots, dev, k)
+                self.v.append(v)
+                self.s.append(s)
+                self.full_loc.append(fl)
+                self.table.append(synth.swa_table(self.full_slots, self.pool_slots, fl, dev, k))
+            self.gpos = torch.arange(G, dtype=torch.int32, device=dev) * r
+            self.cs = synth.rope_table(65536, dev)
+            self.swa_loc = torch.zeros(G, dtype=torch.int32, device=dev)
+            self.launches = 2
+            self.bytes_total = G * (B_TRANSLATE + b_compress(r, payload))
+            self.config["l2"] = f"rotating {self.R} input sets ({self.R * per_set / 2**20:.0f} MB > 129 MB L2)"
+        else:
+            lens = synth.request_lengths(sp["requests"], seed=0)
+            self.gpos = synth.group_positions(lens, r).to(dev)
+            G = self.gpos.numel()
+            self.pool_slots = sp["pool_slots"]
+            v, s = synth.compressor_rows(G * r, dev, 0, score_std=sp["score_std"])
+            self.v, self.s = [v], [s]
+            self.loc = synth.injective_slots(G, self.pool_slots, dev, 0, dtype=torch.int32)
+            self.cs = synth.rope_table(32768, dev)
+            self.bytes_total = G * b_compress(r, payload)
+            self.config.update(groups=G, input_tokens=G * r)
+            self.config["l2"] = f"inputs {G * r * 4096 / 2**30:.2f} GB per step > 129 MB L2"
+        self.G = G
+        self.pool = torch.zeros(self.pool_slots * self.K.bytes_per_token(self.layout),
+                                dtype=torch.uint8, device=dev)
+        self.units = G * r
+        self.bytes_dominant = G * b_compress(r, payload)
+        self.dominant = "compress_kernel"
+
+    def _compress(self, v, s, loc):
+        self.K.kvq_compress(self.layout, 6, self.r, self.K.FLAG_ROPE, v, s, loc, self.pool,
+                            self.pool_slots, cos_sin=self.cs, group_pos=self.gpos, err=self.err)
+
+    def step(self, i):
+        k = i % self.R
+        if self.r == 4:
+            self.K.kvq_translate_loc(self.full_loc[k], self.table[k], self.swa_loc, err=self.err)
+            self._compress(self.v[k], self.s[k], self.swa_loc)
+        else:
+            self._compress(self.v[k], self.s[k], self.loc)
+
+    def dominant_step(self, i):
+        k = i % self.R
+        self._compress(self.v[k], self.s[k], self.swa_loc if self.r == 4 else self.loc)
+
+    def e2e_setup(self):
+        import torch
+        self.hv = self.v[0].cpu().pin_memory()
+        self.hs = self.s[0].cpu().pin_memory()
+        self.dv = torch.empty_like(self.v[0])
+        self.ds = torch.empty_like(self.s[0])
+        self.herr = torch.zeros(1, dtype=torch.int32).pin_memory()
+        h2d = 2 * self.hv.numel() * 4
+        if self.r == 4:
+            self.hloc = self.full_loc[0].cpu().pin_memory()
+            self.dloc = torch.empty_like(self.full_loc[0])
+            h2d += self.hloc.numel() * 8
+        return h2d, 4
+
+    def e2e_step(self):
+        self.dv.copy_(self.hv, non_blocking=True)
+        self.ds.copy_(self.hs, non_blocking=True)
+        if self.r == 4:
+            self.dloc.copy_(self.hloc, non_blocking=True)
+            self.K.kvq_translate_loc(self.dloc, self.table[0], self.swa_loc, err=self.err)
+            loc = self.swa_loc
+        else:
+            loc = self.loc
+        self._compress(self.dv, self.ds, loc)
+        self.herr.copy_(self.err, non_blocking=True)
+
+
+def make_workload(name, dev):
+    kind = SPECS[name]["kind"]
+    cls = {"store": StoreWorkload, "dequant": DequantWorkload, "compress": CompressWorkload}[kind]
+    return cls(name, dev)
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_id), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, ValueError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) != 6:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, p in zip(names, parts[2:]):
+                if p.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def measured_hbm_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def traffic_from_profiles(workload):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu
+    summary, if the kernel sources are unchanged since it was taken."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    try:
+        lines = open(path).read().splitlines()
+    except OSError:
+        return None
+    sha = kernel_source_sha()
+    for ln in lines:
+        p = ln.split()
+        if len(p) >= 4 and not ln.startswith("#") and p[0] == workload and p[3] == sha:
+            return float(p[2])
+    return None
+
+
+def kernel_source_sha():
+    import hashlib
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "compress_kv_write_gb300", "csrc")
+    for fn in sorted(os.listdir(d)):
+        with open(os.path.join(d, fn), "rb") as f:
+            h.update(fn.encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def capture_graphs(wl, steps, chunk, stream):
+    """CUDA graphs holding exactly `steps` steps: (graph, replays) pairs."""
+    import torch
+    plan = []
+    full, rem = divmod(steps, chunk)
+    offset = 0
+    for n, reps in ((chunk, full), (rem, 1)):
+        if n == 0 or reps == 0:
+            continue
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(n):
+                wl.step(offset + i)
+        plan.append((g, reps))
+        offset += n
+    return plan
+
+
+def capture_dominant(wl, n, stream):
+    import torch
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(n):
+            wl.dominant_step(i)
+    return g
+
+
+# ----------------------------------------------------------------------------- arms
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    rank, world, local = dist_env()
+    if world > 1:
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (no CPU path)")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    import __graft_entry__
+    __graft_entry__.build()
+
+    wl = make_workload(args.workload, dev)
+    K = args.steps
+    W = args.warmup
+    stream = torch.cuda.Stream(device=dev)
+
+    # warm-up: W eager steps through the API
+    with torch.cuda.stream(stream):
+        for i in range(W):
+            wl.step(i)
+    stream.synchronize()
+    assert wl.err.item() == 0, "device error during warm-up"
+
+    chunk = min(K, max(wl.R, 1) * max(1, 512 // max(wl.R, 1)))
+    chunk = max(1, chunk)
+    plan = capture_graphs(wl, K, chunk, stream)
+    # one untimed replay uploads the graphs
+    for g, _ in plan:
+        g.replay()
+    stream.synchronize()
+
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    sampler = ClockSampler(vis.split(",")[local] if vis else local)
+    if rank == 0 and not args.no_clocks:
+        sampler.start()
+        time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    with torch.cuda.stream(stream):
+        for g, reps in plan:
+            for _ in range(reps):
+                g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop() if (rank == 0 and not args.no_clocks) else None
+    ms = e0.elapsed_time(e1)
+    assert wl.err.item() == 0, "device error in the timed region"
+    if world > 1:
+        t = torch.tensor([ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_per_step = ms / K
+    units_all = wl.units * K * world
+    value = units_all / (ms / 1e3)
+
+    # dominant kernel alone (for multi-kernel steps), same launch shape
+    if wl.launches > 1:
+        nd = min(K, chunk)
+        gd = capture_dominant(wl, nd, stream)
+        gd.replay()
+        stream.synchronize()
+        d0 = torch.cuda.Event(enable_timing=True)
+        d1 = torch.cuda.Event(enable_timing=True)
+        d0.record(stream)
+        with torch.cuda.stream(stream):
+            gd.replay()
+        d1.record(stream)
+        torch.cuda.synchronize()
+        dom_ms = d0.elapsed_time(d1) / nd
+    else:
+        dom_ms = ms_per_step
+    peak, peak_src = measured_hbm_peak()
+    achieved = wl.bytes_dominant / (dom_ms / 1e3) / 1e9
+    step_gbs = wl.bytes_total / (ms_per_step / 1e3) / 1e9
+
+    # end to end through the API: pinned host inputs -> device, result word back
+    h2d, d2h = wl.e2e_setup()
+    e2e_steps = max(3, min(K, args.e2e_steps))
+    with torch.cuda.stream(stream):
+        wl.e2e_step()
+    stream.synchronize()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for _ in range(e2e_steps):
+            wl.e2e_step()
+    stream.synchronize()
+    e2e_s = time.perf_counter() - t0
+    if world > 1:
+        t = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    e2e_value = wl.units * e2e_steps * world / e2e_s
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(wl.name, args.cpu_seconds)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
+            "warmup": W, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": dict(wl.config, units=wl.unit_name, parallelism=f"replicas{world}",
+                           timing="CUDA graphs of the K steps, CUDA events, 1 untimed upload replay"),
+            "gbs": step_gbs,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "peak_source": f"{peak_src} hbm_gbs (of {peak_src})",
+                         "kernel": wl.dominant, "algorithmic_bytes": wl.bytes_dominant,
+                         "traffic": traffic_from_profiles(wl.name)},
+            "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+            "gpu_launches": wl.launches * K,
+            "clocks": clocks,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def oracle_sample(name, n_rows):
+    """CPU inputs for the oracle, drawn by the same generators (on the CPU)."""
+    import numpy as np
+    import torch
+    from compress_kv_write_gb300 import synth
+    import oracle as O
+    spec = SPECS[name]
+    kind = spec["kind"]
+    if kind == "store":
+        n = n_rows
+        if spec.get("fp32"):
+            x_np = synth.normal((n, 512), "cpu", 0, "x").numpy()
+        elif spec.get("student_t"):
+            x_np = synth.student_t_rows_bf16(n, "cpu", 0).view(torch.int16).numpy().view(np.uint16)
+        else:
+            x_np = synth.store_rows_bf16(n, "cpu", 0).view(torch.int16).numpy().view(np.uint16)
+        return dict(x=x_np, pos=synth.positions(n, "cpu", 0).numpy(),
+                    cs=synth.rope_table(65536, "cpu").numpy(), w=synth.norm_weight("cpu", 0).numpy())
+    if kind == "dequant":
+        n_pages = max(1, n_rows // 64)
+        x_np = synth.student_t_rows_bf16(n_pages * 64, "cpu", 0).view(torch.int16).numpy().view(np.uint16)
+        pool = np.zeros(n_pages * 64 * 288, np.uint8)
+        assert O.store(O.FP4, 6, 0, x_np, np.arange(n_pages * 64), pool) == O.OK
+        return dict(pages=pool)
+    r = spec["ratio"]
+    g = max(1, n_rows // r)
+    v, s = synth.compressor_rows(g * r, "cpu", 0, score_std=spec["score_std"])
+    return dict(v=v.numpy(), s=s.numpy(), gpos=(np.arange(g, dtype=np.int32) * r),
+                cs=synth.rope_table(65536, "cpu").numpy())
+
+
+def oracle_run(name, smp, n_units):
+    """Run the oracle over about n_units tokens of the sample; returns the tokens done."""
+    import numpy as np
+    import oracle as O
+    spec = SPECS[name]
+    kind = spec["kind"]
+    layout = spec.get("layout", 1)
+    if kind == "store":
+        n = min(n_units, smp["x"].shape[0])
+        slots = max(64, -(-n // 64) * 64)
+        pool = np.zeros(slots * O.bytes_per_token(layout), np.uint8)
+        rc = O.store(layout, 6, spec["flags"], smp["x"][:n], np.arange(n), pool, norm_weight=smp["w"],
+                     eps=1e-6, cos_sin=smp["cs"], pos=smp["pos"][:n])
+        assert rc == O.OK
+        return n
+    if kind == "dequant":
+        n_pages = max(1, min(n_units // 64, smp["pages"].size // (64 * 288)))
+        rc, _ = O.dequant(O.FP4, 6, smp["pages"][: n_pages * 64 * 288],
+                          np.arange(n_pages, dtype=np.int32), n_pages * 64)
+        assert rc == O.OK
+        return n_pages * 64
+    r = spec["ratio"]
+    g = max(1, min(n_units // r, smp["gpos"].size))
+    slots = max(64, -(-g // 64) * 64)
+    pool = np.zeros(slots * O.bytes_per_token(layout), np.uint8)
+    rc = O.compress(layout, 6, r, O.ROPE, smp["v"][: g * r], smp["s"][: g * r], np.arange(g), pool,
+                    cos_sin=smp["cs"], group_pos=smp["gpos"][:g])
+    assert rc == O.OK
+    return g * r
+
+
+def _sample_rows(name):
+    spec = SPECS[name]
+    if spec["kind"] == "compress":
+        return spec["ratio"] * (16 if spec["ratio"] >= 128 else 1024)
+    return min(4096, spec.get("bs", 4096))
+
+
+def _chunk_units(name):
+    spec = SPECS[name]
+    if spec["kind"] == "compress":
+        return spec["ratio"] * (1 if spec["ratio"] >= 128 else 64)
+    return min(256, spec.get("bs", 256))
+
+
+def cpu_baseline(name, seconds):
+    """The oracle (single-threaded C) on a bounded sample of the workload."""
+    smp = oracle_sample(name, _sample_rows(name))
+    chunk = _chunk_units(name)
+    done = 0
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < seconds:
+        done += oracle_run(name, smp, chunk)
+    dt = time.perf_counter() - t0
+    return {"value": done / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{done} {describe(name)[1]} of the {name} workload in {dt:.1f} s "
+                      f"(chunks of {chunk}), single-threaded C oracle, gcc -O2"}
+
+
+def run_reference(args):
+    """The CPU oracle as the reference arm, on the same workload and metric.
+    Runs no GPU code; under torchrun only rank 0 works."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle as O
+    O.build()
+    name = args.workload
+    smp = oracle_sample(name, _sample_rows(name))
+    K, W = args.steps, args.warmup
+    chunk = _chunk_units(name)
+    t0 = time.perf_counter()
+    u0 = oracle_run(name, smp, chunk)
+    per_unit = (time.perf_counter() - t0) / u0
+    per_step = int(args.ref_seconds / max(1, K + W) / per_unit)
+    per_step = max(chunk if SPECS[name]["kind"] == "compress" else 1, min(per_step, _sample_rows(name)))
+    for _ in range(W):
+        oracle_run(name, smp, per_step)
+    done = 0
+    t0 = time.perf_counter()
+    for _ in range(K):
+        done += oracle_run(name, smp, per_step)
+    dt = time.perf_counter() - t0
+    value = done / dt
+    config, unit_name = describe(name)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": K, "warmup": W, "ms_per_step": dt * 1e3 / K, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": dict(config, units=unit_name, parallelism="cpu oracle, rank 0 only"),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{done // K} {unit_name} per step of the {name} workload"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default="store_norm_rope",
+                    choices=sorted(DEFAULT_STEPS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--ref-seconds", type=float, default=60.0)
+    ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.steps is None:
+        args.steps = DEFAULT_STEPS[args.workload]
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,469 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
+
+Workloads follow the write path's configurations (see compress_kv_write_gb300.synth):
+the small fp32 V41 store + dequant; the bf16 store / store + RoPE / fused
+norm + RoPE batch sweep; the FP4 store + full-pool paged dequant; the
+translated C4A compressor; the mixed-length C128A compressor (both layouts);
+plus codec sweeps, every compiled instance on ragged sizes, and the error
+paths.  Plain store, RoPE store, scatter, translation and dequant must be
+bit-exact; the norm and pooling paths follow the tolerance rule in
+tests/parity.py.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from parity import (check_tolerance, decode_rows, gather_rows, gather_rows_torch, np_u8)
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module")
+def K():
+    from compress_kv_write_gb300 import build
+    build.build()
+    import compress_kv_write_gb300 as K
+    K.lib()
+    return K
+
+
+def _bf16_np(t):
+    return t.detach().cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+def _err(K):
+    return torch.zeros(1, dtype=torch.int32, device=DEV)
+
+
+def _oracle_store_rows(layout, flags, x_np, norm_weight=None, eps=1e-6, cos_sin=None, pos=None):
+    """Oracle rows of x stored into a compact pool at slots 0..n-1."""
+    n = x_np.shape[0]
+    slots = max(64, -(-n // 64) * 64)
+    pool = np.zeros(slots * O.bytes_per_token(layout), np.uint8)
+    rc = O.store(layout, 6, flags, x_np, np.arange(n), pool, norm_weight=norm_weight, eps=eps,
+                 cos_sin=cos_sin, pos=pos)
+    assert rc == O.OK
+    return gather_rows(pool, layout, 6, np.arange(n))
+
+
+# --------------------------------------------------------------------------- small fp32 config
+
+def test_fp32_store_and_dequant_64_tokens(K):
+    """64 fp32 N(0,1) rows (seed 0) into a 4-page V41 pool at a random
+    injective map of the 256 slots, then the dequant: whole pool and whole
+    workspace bit-exact."""
+    from compress_kv_write_gb300 import synth
+    x = synth.normal((64, 512), "cpu", 0, "x")
+    loc = synth.injective_slots(64, 256, "cpu", 0)
+    pool_o = np.zeros(256 * 528, np.uint8)
+    assert O.store(O.V41, 6, 0, x.numpy(), loc.numpy(), pool_o) == O.OK
+    pool = torch.zeros(256 * 528, dtype=torch.uint8, device=DEV)
+    err = _err(K)
+    K.kvq_store(K.V41, 6, 0, x.to(DEV), loc.to(DEV), pool, 256, err=err)
+    pt = torch.arange(4, dtype=torch.int32)
+    out = torch.full((256, 512), float("nan"), dtype=torch.bfloat16, device=DEV)
+    K.kvq_dequant(K.V41, 6, pool, 4, pt.to(DEV), out, err=err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    assert (np_u8(pool) == pool_o).all()
+    rc, ws = O.dequant(O.V41, 6, pool_o, pt.numpy(), 256)
+    assert rc == O.OK
+    assert (_bf16_np(out) == ws).all()
+
+
+# --------------------------------------------------------------------------- every instance, ragged
+
+@pytest.mark.parametrize("page_bits", [2, 6])
+@pytest.mark.parametrize("layout", [1, 2])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("loc64", [False, True])
+@pytest.mark.parametrize("flags", [0, 1, 2, 3])
+def test_store_instances_ragged(K, page_bits, layout, dtype, loc64, flags):
+    from compress_kv_write_gb300 import synth
+    slots = 1024
+    rng_seed = page_bits * 1000 + layout * 100 + flags * 10 + int(loc64)
+    for n in (1, 37, 301):
+        x = synth.store_rows_bf16(n, "cpu", rng_seed + n)
+        if dtype == "f32":
+            x = x.float() * 1.25          # not bf16-representable in general
+        loc = synth.injective_slots(n, slots, "cpu", rng_seed + n,
+                                    dtype=torch.int64 if loc64 else torch.int32)
+        w = synth.norm_weight("cpu", rng_seed)
+        cs = synth.rope_table(4096, "cpu")
+        pos = synth.positions(n, "cpu", rng_seed + n, max_pos=4096)
+        x_np = x.numpy() if dtype == "f32" else _bf16_np(x)
+        pool_o = np.zeros(slots * O.bytes_per_token(layout), np.uint8)
+        assert O.store(layout, page_bits, flags, x_np, loc.numpy(), pool_o,
+                       norm_weight=w.numpy(), eps=1e-6, cos_sin=cs.numpy(), pos=pos.numpy()) == O.OK
+        pool = torch.zeros(slots * O.bytes_per_token(layout), dtype=torch.uint8, device=DEV)
+        err = _err(K)
+        K.kvq_store(layout, page_bits, flags, x.to(DEV), loc.to(DEV), pool, slots,
+                    norm_weight=w.to(DEV) if flags & 2 else None, eps=1e-6,
+                    cos_sin=cs.to(DEV) if flags & 1 else None,
+                    pos=pos.to(DEV) if flags & 1 else None, err=err)
+        torch.cuda.synchronize()
+        assert err.item() == 0
+        got = np_u8(pool)
+        if flags & 2 == 0:            # plain and RoPE paths: bit-exact
+            assert (got == pool_o).all(), (n, np.flatnonzero(got != pool_o)[:8])
+        else:
+            g = gather_rows(got, layout, page_bits, loc.numpy())
+            o = gather_rows(pool_o, layout, page_bits, loc.numpy())
+            y = np.stack([O.token_prequant(flags, x_np[t], w.numpy(), 1e-6, cs.numpy()[pos[t]])
+                          for t in range(n)])
+            check_tolerance(layout, g[0], g[1], o[0], o[1], y)
+            written = int(g[0].astype(np.int64).sum() + g[1].astype(np.int64).sum())
+            assert int(got.astype(np.int64).sum()) == written   # nothing else touched
+
+
+# --------------------------------------------------------------------------- codecs
+
+def test_codec_every_bf16_pattern(K):
+    """All finite bf16 bit patterns through the plain store, both layouts."""
+    bits = np.arange(65536, dtype=np.uint32)
+    finite = ((bits >> 7) & 0xFF) != 0xFF
+    pat = bits[finite].astype(np.uint16)
+    rng = np.random.default_rng(0)
+    pat = pat[rng.permutation(pat.size)]
+    pad = (-pat.size) % 512
+    pat = np.concatenate([pat, np.zeros(pad, np.uint16)]).reshape(-1, 512)
+    n = pat.shape[0]
+    x = torch.from_numpy(pat.view(np.int16)).view(torch.bfloat16).to(DEV)
+    for layout in (1, 2):
+        rows_o = _oracle_store_rows(layout, 0, pat)
+        pool = torch.zeros(256 * O.bytes_per_token(layout), dtype=torch.uint8, device=DEV)
+        loc = torch.arange(n, dtype=torch.int32, device=DEV)
+        K.kvq_store(layout, 6, 0, x, loc, pool, 256)
+        torch.cuda.synchronize()
+        g = gather_rows(np_u8(pool), layout, 6, np.arange(n))
+        assert (g[0] == rows_o[0]).all() and (g[1] == rows_o[1]).all()
+
+
+def _midpoint_rows(anchor, grid):
+    """fp32 rows whose blocks start with `anchor` (pinning the block scale) and
+    hold the grid's midpoints and their neighbours, both signs."""
+    mids = ((grid[1:] + grid[:-1]) / 2).astype(np.float32)
+    vals = np.concatenate([mids, np.nextafter(mids, np.float32(0)),
+                           np.nextafter(mids, np.float32(1e30)), grid.astype(np.float32)])
+    vals = np.concatenate([vals, -vals])
+    per = 31
+    nblk = -(-vals.size // per)
+    vals = np.concatenate([vals, np.zeros(nblk * per - vals.size, np.float32)]).reshape(nblk, per)
+    blocks = np.concatenate([np.full((nblk, 1), anchor, np.float32), vals], axis=1)
+    nb = -(-nblk // 16) * 16
+    blocks = np.concatenate([blocks, np.zeros((nb - nblk, 32), np.float32)])
+    return blocks.reshape(-1, 512)
+
+
+def test_codec_e4m3_midpoints(K):
+    codes = np.array([c for c in range(128) if c != 0x7F], np.uint8)
+    grid = np.unique(O.e4m3_decode(codes))
+    x = _midpoint_rows(448.0, grid)          # byte 127: multiplier 1
+    x = np.concatenate([x, _midpoint_rows(511.0, np.array([448.0, 460.0, 464.0, 480.0, 500.0]))])
+    rows_o = _oracle_store_rows(O.V41, 0, x)
+    n = x.shape[0]
+    pool = torch.zeros(-(-n // 64) * 64 * 528, dtype=torch.uint8, device=DEV)
+    K.kvq_store(K.V41, 6, 0, torch.from_numpy(x).to(DEV), torch.arange(n, device=DEV), pool,
+                -(-n // 64) * 64)
+    torch.cuda.synchronize()
+    g = gather_rows(np_u8(pool), O.V41, 6, np.arange(n))
+    assert (g[1] == rows_o[1]).all()
+    assert (g[0] == rows_o[0]).all(), np.argwhere(g[0] != rows_o[0])[:5]
+
+
+def test_codec_e2m1_midpoints(K):
+    grid = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6], np.float64)
+    x = _midpoint_rows(6.0, grid)            # scale 1.0
+    x = np.concatenate([x, _midpoint_rows(6.0, np.array([5.9, 6.0, 6.2, 7.0, 100.0]))])
+    x = np.clip(x, -6, 6)                    # keep the block amax at 6
+    rows_o = _oracle_store_rows(O.FP4, 0, x)
+    n = x.shape[0]
+    slots = -(-n // 64) * 64
+    pool = torch.zeros(slots * 288, dtype=torch.uint8, device=DEV)
+    K.kvq_store(K.V41_FP4, 6, 0, torch.from_numpy(x).to(DEV), torch.arange(n, device=DEV), pool, slots)
+    torch.cuda.synchronize()
+    g = gather_rows(np_u8(pool), O.FP4, 6, np.arange(n))
+    assert (g[1] == rows_o[1]).all()
+    assert (g[0] == rows_o[0]).all()
+
+
+@pytest.mark.parametrize("layout", [1, 2])
+def test_codec_dequant_every_code_and_scale(K, layout):
+    """Every (code, scale byte) pair through the paged dequant."""
+    P = 64
+    bpt = O.bytes_per_token(layout)
+    pool = np.zeros(P * bpt, np.uint8)
+    cb, sb = (512, 16) if layout == 1 else (256, 32)
+    for t in range(P):
+        pool[t * cb:(t + 1) * cb] = (np.arange(cb) + 7 * t) % 256
+        s = (np.arange(16) + 16 * t) % 256
+        pool[P * cb + t * sb:P * cb + t * sb + 16] = s
+    out = torch.empty((P, 512), dtype=torch.bfloat16, device=DEV)
+    K.kvq_dequant(layout, 6, torch.from_numpy(pool).to(DEV), 1,
+                  torch.zeros(1, dtype=torch.int32, device=DEV), out)
+    torch.cuda.synchronize()
+    rc, ws = O.dequant(layout, 6, pool, np.zeros(1, np.int32), P)
+    got = _bf16_np(out)
+    gf = O.bf16_to_f32(got)
+    of = O.bf16_to_f32(ws)
+    nan = np.isnan(of)
+    assert (np.isnan(gf) == nan).all()
+    assert (got[~nan] == ws[~nan]).all()
+
+
+# --------------------------------------------------------------------------- store batch sweep
+
+POOL_SLOTS_1 = 1 << 20
+
+
+@pytest.fixture(scope="module")
+def sweep_inputs():
+    from compress_kv_write_gb300 import synth
+    n = 16384
+    x = synth.store_rows_bf16(n, DEV, 0)
+    loc = synth.injective_slots(n, POOL_SLOTS_1, DEV, 0)
+    pos = synth.positions(n, DEV, 0)
+    cs = synth.rope_table(65536, DEV)
+    w = synth.norm_weight(DEV, 0)
+    return x, loc, pos, cs, w
+
+
+@pytest.mark.parametrize("bs", [1, 8, 64, 512, 16384])
+@pytest.mark.parametrize("flags", [0, 1, 3])
+def test_store_batch_sweep(K, sweep_inputs, bs, flags):
+    """bf16 rows with outliers, pool of 2^20 slots: store, store + RoPE and
+    fused K RMSNorm + RoPE at every batch size of the sweep."""
+    x, loc, pos, cs, w = sweep_inputs
+    x, loc, pos = x[:bs], loc[:bs], pos[:bs]
+    pool = torch.zeros(POOL_SLOTS_1 * 528, dtype=torch.uint8, device=DEV)
+    err = _err(K)
+    K.kvq_store(K.V41, 6, flags, x, loc, pool, POOL_SLOTS_1, norm_weight=w, eps=1e-6,
+                cos_sin=cs, pos=pos, err=err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    g = gather_rows_torch(pool, O.V41, 6, loc.cpu().numpy())
+    x_np, pos_np, cs_np, w_np = _bf16_np(x), pos.cpu().numpy(), cs.cpu().numpy(), w.cpu().numpy()
+    o = _oracle_store_rows(O.V41, flags, x_np, w_np, 1e-6, cs_np, pos_np)
+    if flags & 2:
+        y = np.stack([O.token_prequant(flags, x_np[t], w_np, 1e-6, cs_np[pos_np[t]]) for t in range(bs)])
+        check_tolerance(O.V41, g[0], g[1], o[0], o[1], y)
+    else:
+        assert (g[0] == o[0]).all() and (g[1] == o[1]).all()
+    written = int(g[0].astype(np.int64).sum() + g[1].astype(np.int64).sum())
+    assert int(pool.sum(dtype=torch.int64).item()) == written
+
+
+# --------------------------------------------------------------------------- FP4 store + dequant
+
+POOL_SLOTS_2 = 1 << 21
+
+
+@pytest.mark.parametrize("bs", [16384, 262144])
+def test_fp4_store_and_full_pool_dequant(K, bs):
+    """Student-t(3) x 0.5 bf16 rows into a 2^21-slot FP4 pool, then the paged
+    dequant of the whole pool through a permuted page table."""
+    from compress_kv_write_gb300 import synth
+    x = synth.student_t_rows_bf16(bs, DEV, 0)
+    loc = synth.injective_slots(bs, POOL_SLOTS_2, DEV, 0)
+    pool = torch.zeros(POOL_SLOTS_2 * 288, dtype=torch.uint8, device=DEV)
+    err = _err(K)
+    K.kvq_store(K.V41_FP4, 6, 0, x, loc, pool, POOL_SLOTS_2, err=err)
+    n_pages = POOL_SLOTS_2 >> 6
+    pt = synth.page_table_perm(n_pages, DEV, 0)
+    out = torch.empty((POOL_SLOTS_2, 512), dtype=torch.bfloat16, device=DEV)
+    K.kvq_dequant(K.V41_FP4, 6, pool, n_pages, pt, out, err=err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    # every stored row, bit-exact
+    loc_np = loc.cpu().numpy()
+    g = gather_rows_torch(pool, O.FP4, 6, loc_np)
+    o = _oracle_store_rows(O.FP4, 0, _bf16_np(x))
+    assert (g[0] == o[0]).all() and (g[1] == o[1]).all()
+    written = int(g[0].astype(np.int64).sum() + g[1].astype(np.int64).sum())
+    assert int(pool.sum(dtype=torch.int64).item()) == written
+    # dequant: sampled logical pages, oracle on the gathered physical pages
+    rng = np.random.default_rng(bs)
+    pt_np = pt.cpu().numpy()
+    lps = rng.choice(n_pages, 96, replace=False)
+    # make sure some sampled pages hold stored rows
+    lps = np.unique(np.concatenate([lps, np.flatnonzero(np.isin(pt_np, loc_np[:32] >> 6))]))
+    pb = 64 * 288
+    page_bytes = torch.stack([pool[int(p) * pb:(int(p) + 1) * pb] for p in pt_np[lps]]).cpu().numpy()
+    rc, ws = O.dequant(O.FP4, 6, page_bytes.reshape(-1), np.arange(lps.size, dtype=np.int32), lps.size * 64)
+    assert rc == O.OK
+    rows = (lps[:, None] * 64 + np.arange(64)[None, :]).reshape(-1)
+    got = _bf16_np(out[torch.as_tensor(rows, device=DEV)])
+    assert (got == ws).all()
+    assert np.count_nonzero(ws) > 0
+
+
+# --------------------------------------------------------------------------- C4A + translation
+
+def test_translate_and_c4a(K):
+    """65536 fp32 rows (values N(0,1), scores N(0,2)) in 16384 groups of 4;
+    out_cache_loc injective into a 2^20-slot full pool, translated once to
+    a 2^17-slot SWA pool; RoPE at positions 4g; V41 store."""
+    from compress_kv_write_gb300 import synth
+    G, r = 16384, 4
+    full_slots, swa_slots = 1 << 20, 1 << 17
+    v, s = synth.compressor_rows(G * r, DEV, 0, score_std=math.sqrt(2.0))
+    full_loc = synth.injective_slots(G, full_slots, DEV, 0)
+    table = synth.swa_table(full_slots, swa_slots, full_loc, DEV, 0)
+    cap = G + 1000
+    swa_loc = torch.full((cap,), 12345, dtype=torch.int32, device=DEV)
+    err = _err(K)
+    K.kvq_translate_loc(full_loc, table, swa_loc, err=err)
+    gpos = (torch.arange(G, dtype=torch.int32, device=DEV) * r)
+    cs = synth.rope_table(65536, DEV)
+    pool = torch.zeros(swa_slots * 528, dtype=torch.uint8, device=DEV)
+    K.kvq_compress(K.V41, 6, r, K.FLAG_ROPE, v, s, swa_loc[:G], pool, swa_slots, cos_sin=cs,
+                   group_pos=gpos, err=err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    rc, tr = O.translate(full_loc.cpu().numpy(), table.cpu().numpy(), cap)
+    assert rc == O.OK
+    assert (swa_loc.cpu().numpy() == tr).all()
+    slots = tr[:G]
+    assert np.unique(slots).size == G
+    v_np, s_np, cs_np = v.cpu().numpy(), s.cpu().numpy(), cs.cpu().numpy()
+    pool_o = np.zeros(swa_slots * 528, np.uint8)
+    rc = O.compress(O.V41, 6, r, O.ROPE, v_np, s_np, slots, pool_o, cos_sin=cs_np,
+                    group_pos=gpos.cpu().numpy())
+    assert rc == O.OK
+    got = np_u8(pool)
+    g = gather_rows(got, O.V41, 6, slots)
+    o = gather_rows(pool_o, O.V41, 6, slots)
+    y = np.stack([O.group_prequant(r, O.ROPE, v_np[i * r:(i + 1) * r], s_np[i * r:(i + 1) * r],
+                                   cs_np[i * r]) for i in range(G)])
+    check_tolerance(O.V41, g[0], g[1], o[0], o[1], y)
+    written = int(g[0].astype(np.int64).sum() + g[1].astype(np.int64).sum())
+    assert int(got.astype(np.int64).sum()) == written
+
+
+@pytest.mark.parametrize("layout", [1, 2])
+@pytest.mark.parametrize("r", [1, 2, 4, 128])
+def test_compress_small_exhaustive(K, layout, r):
+    """Every compiled ratio, ragged group counts, whole-pool comparison."""
+    from compress_kv_write_gb300 import synth
+    slots = 512
+    for G in (1, 3, 45):
+        v, s = synth.compressor_rows(G * r, "cpu", G + r, score_std=2.0)
+        loc = synth.injective_slots(G, slots, "cpu", G, dtype=torch.int32)
+        gpos = synth.positions(G, "cpu", G, max_pos=1024)
+        cs = synth.rope_table(1024, "cpu")
+        pool_o = np.zeros(slots * O.bytes_per_token(layout), np.uint8)
+        assert O.compress(layout, 6, r, O.ROPE, v.numpy(), s.numpy(), loc.numpy(), pool_o,
+                          cos_sin=cs.numpy(), group_pos=gpos.numpy()) == O.OK
+        pool = torch.zeros_like(torch.from_numpy(pool_o), device=DEV)
+        err = _err(K)
+        K.kvq_compress(layout, 6, r, K.FLAG_ROPE, v.to(DEV), s.to(DEV), loc.to(DEV), pool, slots,
+                       cos_sin=cs.to(DEV), group_pos=gpos.to(DEV), err=err)
+        torch.cuda.synchronize()
+        assert err.item() == 0
+        got = np_u8(pool)
+        gs = loc.numpy()
+        g = gather_rows(got, layout, 6, gs)
+        o = gather_rows(pool_o, layout, 6, gs)
+        gp = gpos.numpy()
+        y = np.stack([O.group_prequant(r, O.ROPE, v.numpy()[i * r:(i + 1) * r], s.numpy()[i * r:(i + 1) * r],
+                                       cs.numpy()[gp[i]]) for i in range(G)])
+        if r == 1:   # r = 1 pooling is the identity: bit-exact
+            assert (g[0] == o[0]).all() and (g[1] == o[1]).all()
+        else:
+            check_tolerance(layout, g[0], g[1], o[0], o[1], y, budget=2e-3 if G * 512 < 5000 else 1e-3)
+        written = int(g[0].astype(np.int64).sum() + g[1].astype(np.int64).sum())
+        assert int(got.astype(np.int64).sum()) == written
+
+
+# --------------------------------------------------------------------------- C128A mixed batch
+
+@pytest.mark.parametrize("layout", [1, 2])
+def test_c128a_mixed_batch(K, layout):
+    """256 requests, log-uniform lengths in [128, 32768] (multiples of 128),
+    values N(0,1), scores N(0,4); 128-row groups at positions 128 * local
+    group index; sampled groups against the oracle."""
+    from compress_kv_write_gb300 import synth
+    r = 128
+    lens = synth.request_lengths(256, seed=0)
+    gpos = synth.group_positions(lens, r).to(DEV)
+    G = gpos.numel()
+    pool_slots = 1 << 20
+    v, s = synth.compressor_rows(G * r, DEV, 0, score_std=2.0)
+    loc = synth.injective_slots(G, pool_slots, DEV, 0, dtype=torch.int32)
+    cs = synth.rope_table(32768, DEV)
+    pool = torch.zeros(pool_slots * O.bytes_per_token(layout), dtype=torch.uint8, device=DEV)
+    err = _err(K)
+    K.kvq_compress(layout, 6, r, K.FLAG_ROPE, v, s, loc, pool, pool_slots, cos_sin=cs,
+                   group_pos=gpos, err=err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    rng = np.random.default_rng(layout)
+    pick = np.unique(np.concatenate([rng.choice(G, 150, replace=False), [0, G - 1]]))
+    loc_np, gpos_np, cs_np = loc.cpu().numpy(), gpos.cpu().numpy(), cs.cpu().numpy()
+    g = gather_rows_torch(pool, layout, 6, loc_np[pick])
+    oc, osc, ys = [], [], []
+    for i in pick:
+        vi = v[i * r:(i + 1) * r].cpu().numpy()
+        si = s[i * r:(i + 1) * r].cpu().numpy()
+        c, sc = O.group_bytes(layout, r, O.ROPE, vi, si, cs_np[gpos_np[i]])
+        oc.append(c)
+        osc.append(sc)
+        ys.append(O.group_prequant(r, O.ROPE, vi, si, cs_np[gpos_np[i]]))
+    check_tolerance(layout, g[0], g[1], np.stack(oc), np.stack(osc), np.stack(ys))
+    # every group was written: its scale row is non-zero
+    gs = gather_rows_torch(pool, layout, 6, loc_np)[1]
+    assert (gs[:, :16].astype(np.int64).sum(1) > 0).all()
+
+
+# --------------------------------------------------------------------------- error paths
+
+def test_error_paths(K):
+    from compress_kv_write_gb300 import synth
+    x = synth.store_rows_bf16(4, DEV, 1)
+    pool = torch.zeros(64 * 528, dtype=torch.uint8, device=DEV)
+    # n = 0 enqueues nothing
+    K.kvq_store(K.V41, 6, 0, x[:0], torch.zeros(0, dtype=torch.int64, device=DEV), pool, 64)
+    # out-of-range slots: flagged and skipped, the other rows written
+    err = _err(K)
+    loc = torch.tensor([3, 64, -5, 7], device=DEV)
+    K.kvq_store(K.V41, 6, 0, x, loc, pool, 64, err=err)
+    torch.cuda.synchronize()
+    assert err.item() == K.kvq.DEVERR_SLOT
+    ref = np.zeros(64 * 528, np.uint8)
+    O.store(O.V41, 6, 0, _bf16_np(x), np.array([3, 64, -5, 7]), ref)
+    assert (np_u8(pool) == ref).all()
+    # out-of-range RoPE position
+    err.zero_()
+    pool.zero_()
+    cs = synth.rope_table(16, DEV)
+    K.kvq_store(K.V41, 6, K.FLAG_ROPE, x, torch.tensor([0, 1, 2, 3], device=DEV), pool, 64,
+                cos_sin=cs, pos=torch.tensor([0, 16, 3, -1], dtype=torch.int32, device=DEV), err=err)
+    torch.cuda.synchronize()
+    assert err.item() == K.kvq.DEVERR_POS
+    g = gather_rows(np_u8(pool), O.V41, 6, np.arange(4))
+    assert (g[1][[1, 3]] == 0).all() and (g[1][[0, 2]] != 0).any()
+    # bad page-table entry: flagged, that page untouched
+    err.zero_()
+    out = torch.full((128, 512), 7.0, dtype=torch.bfloat16, device=DEV)
+    K.kvq_dequant(K.V41, 6, pool, 1, torch.tensor([0, 1], dtype=torch.int32, device=DEV), out, err=err)
+    torch.cuda.synchronize()
+    assert err.item() == K.kvq.DEVERR_PAGE
+    assert (out[64:] == 7.0).all()
+    # translation: capacity error enqueues nothing; bad locs -> -1
+    outb = torch.full((4,), 99, dtype=torch.int32, device=DEV)
+    with pytest.raises(K.KVQError) as e:
+        K.kvq_translate_loc(torch.arange(5, device=DEV), torch.arange(8, dtype=torch.int32, device=DEV), outb)
+    assert e.value.status == K.kvq.ERR_CAPACITY
+    torch.cuda.synchronize()
+    assert (outb == 99).all()
+    err.zero_()
+    K.kvq_translate_loc(torch.tensor([1, 9, -1], dtype=torch.int32, device=DEV),
+                        torch.arange(8, dtype=torch.int32, device=DEV) * 2, outb, err=err)
+    torch.cuda.synchronize()
+    assert outb.cpu().tolist() == [2, -1, -1, 0]
+    assert err.item() == K.kvq.DEVERR_LOC
