@@ -211,6 +211,7 @@ extern "C" kvq_status kvq_compress(kvq_layout layout, int page_bits, int ratio, 
     if (ratio < 1) return KVQ_ERR_INVALID_ARG;
     if (ratio != 1 && ratio != 2 && ratio != 4 && ratio != 128) return KVQ_ERR_UNSUPPORTED;
     if (n_groups < 0) return KVQ_ERR_INVALID_ARG;
+    if (n_groups == 0) return KVQ_OK;  // nothing to enqueue; inputs may be empty (null)
     if (!values || !scores || !aligned(values, 16) || !aligned(scores, 16)) return KVQ_ERR_INVALID_ARG;
     if (!loc || !aligned(loc, 4)) return KVQ_ERR_INVALID_ARG;
     const bool rope = flags & KVQ_FLAG_ROPE;
@@ -218,7 +219,6 @@ extern "C" kvq_status kvq_compress(kvq_layout layout, int page_bits, int ratio, 
                  !aligned(group_pos, 4)))
         return KVQ_ERR_INVALID_ARG;
     if (err && !aligned(err, 4)) return KVQ_ERR_INVALID_ARG;
-    if (n_groups == 0) return KVQ_OK;
 
     CompressArgs a;
     a.values = values;

@@ -122,11 +122,11 @@ extern "C" kvq_status kvq_dequant(kvq_layout layout, int page_bits, const uint8_
     if (!page_bits_supported(page_bits)) return KVQ_ERR_UNSUPPORTED;
     if (!pool || !aligned(pool, 16) || pool_pages <= 0) return KVQ_ERR_INVALID_ARG;
     if (n_tokens < 0 || (n_tokens & ((int64_t(1) << page_bits) - 1)) != 0) return KVQ_ERR_INVALID_ARG;
+    if (n_tokens == 0) return KVQ_OK;  // nothing to enqueue; the table / output may be empty
     if (!page_table || !aligned(page_table, 4)) return KVQ_ERR_INVALID_ARG;
     if (!out_bf16 || !aligned(out_bf16, 16) || out_row_stride < kD || (out_row_stride * 2) % 16 != 0)
         return KVQ_ERR_INVALID_ARG;
     if (err && !aligned(err, 4)) return KVQ_ERR_INVALID_ARG;
-    if (n_tokens == 0) return KVQ_OK;
 
     DequantArgs a;
     a.pool = pool;

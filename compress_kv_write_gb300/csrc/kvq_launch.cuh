@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <type_traits>
 
 #include "kvq_device.cuh"
@@ -16,12 +17,12 @@ inline bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintp
 // Launch with programmatic stream serialisation, so a kernel can start its
 // prologue while its predecessor drains (it waits with griddepcontrol.wait).
 template <typename... KArgs, typename... Args>
-kvq_status launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, cudaStream_t stream,
-                      Args &&...args) {
+kvq_status launch_pdl_smem(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                           cudaStream_t stream, Args &&...args) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;
-    cfg.dynamicSmemBytes = 0;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -33,6 +34,45 @@ kvq_status launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, cudaStrea
         (void)cudaGetLastError();
         return KVQ_ERR_LAUNCH;
     }
+    return KVQ_OK;
+}
+
+template <typename... KArgs, typename... Args>
+kvq_status launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, cudaStream_t stream,
+                      Args &&...args) {
+    return launch_pdl_smem(kernel, grid, block, 0, stream, std::forward<Args>(args)...);
+}
+
+// Per-device launch limits of a kernel instance: opts it into `smem` bytes of
+// dynamic shared memory (once per device) and returns the largest grid that
+// is resident at once (blocks per SM x SMs).
+constexpr int kMaxDevices = 64;
+
+template <auto Kernel>
+kvq_status resident_grid(int threads, size_t smem, int64_t *grid_cap) {
+    static std::atomic<int> cap[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        (void)cudaGetLastError();
+        return KVQ_ERR_LAUNCH;
+    }
+    int c = cap[dev].load(std::memory_order_relaxed);
+    if (c == 0) {
+        if (smem > 48 * 1024 &&
+            cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return KVQ_ERR_LAUNCH;
+        }
+        int bps = 0, sms = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, Kernel, threads, smem) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return KVQ_ERR_LAUNCH;
+        }
+        c = (bps > 0 ? bps : 1) * (sms > 0 ? sms : 1);
+        cap[dev].store(c, std::memory_order_relaxed);
+    }
+    *grid_cap = c;
     return KVQ_OK;
 }
 

@@ -69,7 +69,9 @@ enum {
     KVQ_DEVERR_SLOT = 1,  /* a slot outside [0, pool_slots) (row skipped)        */
     KVQ_DEVERR_POS = 2,   /* a RoPE position outside [0, cos_sin_rows) (skipped) */
     KVQ_DEVERR_PAGE = 4,  /* a page-table entry outside [0, pool_pages) (skipped)*/
-    KVQ_DEVERR_LOC = 8    /* a full slot outside the translation table (-> -1)   */
+    KVQ_DEVERR_LOC = 8,   /* a full slot outside the translation table (-> -1)   */
+    KVQ_DEVERR_TIMEOUT = 16 /* an internal pipeline wait ran past its 2 s limit;  */
+                            /* the kernel stopped early (output incomplete)       */
 };
 
 /* Bytes one token occupies: 528 (V41) or 288 (V41_FP4); 0 for a bad layout.

@@ -72,6 +72,7 @@ def test_store_rejects_on_host(L):
     assert _store(L, flags=1, cs=A, rows=0, pos=A) == 1
     assert _store(L, flags=1, cs=A, rows=8, pos=None) == 1
     assert _store(L, n=0) == 0                   # nothing to do: no launch
+    assert _store(L, n=0, x=None, loc=None) == 0  # empty inputs may be null
 
 
 def test_compress_rejects_on_host(L):
