@@ -335,7 +335,19 @@ class CompressWorkload(Workload):
         self.herr.copy_(self.err, non_blocking=True)
 
 
-def make_workload(name, dev):
+def make_workload(name, dev, tokens=None):
+    """tokens (profiling only): shrink the workload to about this many KV tokens."""
+    if tokens:
+        sp = dict(SPECS[name])
+        if sp["kind"] == "store":
+            sp["bs"] = int(tokens)
+        elif sp["kind"] == "dequant":
+            sp["pool_slots"] = max(1 << 18, (int(tokens) >> 18) << 18)
+        elif sp["ratio"] == 4:
+            sp["groups"] = max(1, int(tokens) // 4)
+        else:
+            sp["requests"] = max(1, int(tokens) * 256 // 1_500_000)
+        SPECS[name] = sp
     kind = SPECS[name]["kind"]
     cls = {"store": StoreWorkload, "dequant": DequantWorkload, "compress": CompressWorkload}[kind]
     return cls(name, dev)
@@ -488,7 +500,7 @@ def run_ours(args):
     import __graft_entry__
     __graft_entry__.build()
 
-    wl = make_workload(args.workload, dev)
+    wl = make_workload(args.workload, dev, args.tokens)
     K = args.steps
     W = args.warmup
     stream = torch.cuda.Stream(device=dev)
@@ -504,9 +516,10 @@ def run_ours(args):
     chunk = max(1, chunk)
     plan = capture_graphs(wl, K, chunk, stream)
     # one untimed replay uploads the graphs
-    for g, _ in plan:
-        g.replay()
-    stream.synchronize()
+    with torch.cuda.stream(stream):
+        for g, _ in plan:
+            g.replay()
+    torch.cuda.synchronize()
 
     vis = os.environ.get("CUDA_VISIBLE_DEVICES")
     sampler = ClockSampler(vis.split(",")[local] if vis else local)
@@ -542,8 +555,9 @@ def run_ours(args):
     if wl.launches > 1:
         nd = min(K, chunk)
         gd = capture_dominant(wl, nd, stream)
-        gd.replay()
-        stream.synchronize()
+        with torch.cuda.stream(stream):
+            gd.replay()
+        torch.cuda.synchronize()
         d0 = torch.cuda.Event(enable_timing=True)
         d1 = torch.cuda.Event(enable_timing=True)
         d0.record(stream)
@@ -747,6 +761,8 @@ def main(argv=None):
     ap.add_argument("--ref-seconds", type=float, default=60.0)
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="profiling only: shrink the workload to about this many tokens")
     args = ap.parse_args(argv)
     if args.steps is None:
         args.steps = DEFAULT_STEPS[args.workload]

@@ -2,13 +2,13 @@
 // bf16 workspace, the job of dequant_k_cache.py in "[sglang] DeepSeek V4.1
 // Paged KV Cache: V41 and FP4 formats" (section 4).
 //
-// Mapping: one CTA per logical page.  The page's code area is contiguous, so
-// the CTA sweeps it in 16-byte chunks (thread i takes chunks i, i+256, ...),
-// all loads issued before any conversion; each chunk's scale byte comes from
-// the page's scale area.  V41: a chunk is 16 codes of one row (half a quant
-// block) -> 32 bytes of bf16.  V41_FP4: a chunk is one whole 32-value block
-// -> 64 bytes of bf16.  Every product code * scale has at most 6 significant
-// bits, so the bf16 result is exact.
+// Mapping: one CTA per logical page.  The page's code area is cut into
+// pieces of 8 values (8 bytes of e4m3 or 4 bytes of e2m1); thread i takes
+// pieces i, i+256, ...  Each piece becomes 16 bytes of bf16, so the 32 lanes
+// of a warp write 512 contiguous bytes per store instruction.  Every code
+// load of the CTA is issued first; the page's scale rows are staged in
+// shared memory meanwhile.  Every product code * scale has at most 6
+// significant bits, so the bf16 result is exact.
 #include "kvq_launch.cuh"
 
 namespace kvq {
@@ -25,20 +25,20 @@ struct DequantArgs {
     int32_t *err;
 };
 
-__device__ __forceinline__ uint8_t ld_byte(const uint8_t *p) {
-    uint16_t r;
-    asm volatile("ld.global.nc.u8 %0, [%1];" : "=h"(r) : "l"(p));
-    return uint8_t(r);
-}
-
 template <Layout L, int PageBits>
 __global__ void __launch_bounds__(kDqThreads) dequant_kernel(const DequantArgs a) {
     using PK = PagedKV<L, PageBits>;
     using T = LayoutTraits<L>;
     constexpr int64_t P = PK::kPage;
-    constexpr int kChunksPerRow = T::kCodeBytes / 16;       // 32 (V41) or 16 (FP4)
-    constexpr int64_t kChunks = P * kChunksPerRow;
-    constexpr int ITER = int((kChunks + kDqThreads - 1) / kDqThreads);
+    constexpr int kPieceBytes = L == Layout::V41 ? 8 : 4;        // 8 values
+    constexpr int kPiecesPerRow = T::kCodeBytes / kPieceBytes;     // 64
+    constexpr int64_t kPieces = P * kPiecesPerRow;
+    constexpr int ITER = int((kPieces + kDqThreads - 1) / kDqThreads);
+    constexpr int kScaleArea = int(P * T::kScaleBytes);           // bytes
+    static_assert(kPiecesPerRow == 64, "a row is 64 pieces of 8 values");
+    static_assert(kScaleArea % 16 == 0, "scale area is whole 16-byte chunks");
+
+    __shared__ __align__(16) uint8_t s_scale[kScaleArea];
 
     const int64_t lp = blockIdx.x;
     pdl_wait();
@@ -50,55 +50,54 @@ __global__ void __launch_bounds__(kDqThreads) dequant_kernel(const DequantArgs a
     const uint8_t *codes = a.pool + phys * PK::kPageBytes;
     const uint8_t *scales = codes + P * T::kCodeBytes;
 
-    uint4 raw[ITER];
-    uint8_t sb[ITER];
+    uint2 raw[ITER];
 #pragma unroll
     for (int it = 0; it < ITER; ++it) {
-        const int64_t c = int64_t(it) * kDqThreads + threadIdx.x;
-        if (c < kChunks) {
-            raw[it] = ld_stream_u4(codes + c * 16);
-            const int64_t row = c / kChunksPerRow;
-            const int blk = L == Layout::V41 ? int(c % kChunksPerRow) / 2 : int(c % kChunksPerRow);
-            sb[it] = ld_byte(scales + row * T::kScaleBytes + blk);
+        const int64_t q = int64_t(it) * kDqThreads + threadIdx.x;
+        if (q < kPieces) {
+            if constexpr (kPieceBytes == 8) {
+                raw[it] = __ldg(reinterpret_cast<const uint2 *>(codes) + q);
+            } else {
+                raw[it].x = __ldg(reinterpret_cast<const uint32_t *>(codes) + q);
+                raw[it].y = 0;
+            }
         }
     }
+    for (int c = threadIdx.x; c < kScaleArea / 16; c += kDqThreads)
+        *reinterpret_cast<uint4 *>(s_scale + c * 16) = __ldg(reinterpret_cast<const uint4 *>(scales) + c);
+    __syncthreads();
     pdl_trigger();
 
 #pragma unroll
     for (int it = 0; it < ITER; ++it) {
-        const int64_t c = int64_t(it) * kDqThreads + threadIdx.x;
-        if (c >= kChunks) break;
-        const int64_t row = c / kChunksPerRow;
-        const int j = int(c % kChunksPerRow);
-        uint8_t *orow = a.out + (lp * P + row) * a.out_stride_bytes;
-        const uint32_t w[4] = {raw[it].x, raw[it].y, raw[it].z, raw[it].w};
+        const int64_t q = int64_t(it) * kDqThreads + threadIdx.x;
+        if (q >= kPieces) break;
+        const int64_t row = q / kPiecesPerRow;
+        const int j = int(q % kPiecesPerRow);                 // values 8j .. 8j+7
+        const uint32_t sb = s_scale[row * T::kScaleBytes + j / 4];
+        uint32_t o[4];
         if constexpr (L == Layout::V41) {
-            const float sc = ue8m0_to_f32(sb[it]);
-            uint32_t o[8];
+            const float sc = ue8m0_to_f32(sb);
+            const uint32_t w[2] = {raw[it].x, raw[it].y};
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const float2 f0 = e4m3x2_to_f32x2(w[q] & 0xFFFFu);
-                const float2 f1 = e4m3x2_to_f32x2(w[q] >> 16);
-                o[2 * q] = pack_bf16x2(__fmul_rn(f0.x, sc), __fmul_rn(f0.y, sc));
-                o[2 * q + 1] = pack_bf16x2(__fmul_rn(f1.x, sc), __fmul_rn(f1.y, sc));
+            for (int h = 0; h < 2; ++h) {
+                const float2 f0 = e4m3x2_to_f32x2(w[h] & 0xFFFFu);
+                const float2 f1 = e4m3x2_to_f32x2(w[h] >> 16);
+                const float2 g0 = fmul2(f0, make_float2(sc, sc));
+                const float2 g1 = fmul2(f1, make_float2(sc, sc));
+                o[2 * h] = pack_bf16x2(g0.x, g0.y);
+                o[2 * h + 1] = pack_bf16x2(g1.x, g1.y);
             }
-            st_u4(orow + j * 32, make_uint4(o[0], o[1], o[2], o[3]));
-            st_u4(orow + j * 32 + 16, make_uint4(o[4], o[5], o[6], o[7]));
         } else {
-            const float S = e4m3x2_to_f32x2(sb[it]).x;
-            uint32_t o[16];
+            const float S = e4m3x2_to_f32x2(sb).x;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-#pragma unroll
-                for (int b = 0; b < 4; ++b) {
-                    const float2 f = e2m1x2_to_f32x2((w[q] >> (8 * b)) & 0xFFu);
-                    o[4 * q + b] = pack_bf16x2(__fmul_rn(f.x, S), __fmul_rn(f.y, S));
-                }
+            for (int b = 0; b < 4; ++b) {
+                const float2 f = e2m1x2_to_f32x2((raw[it].x >> (8 * b)) & 0xFFu);
+                const float2 g = fmul2(f, make_float2(S, S));
+                o[b] = pack_bf16x2(g.x, g.y);
             }
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-                st_u4(orow + j * 64 + 16 * q, make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]));
         }
+        st_u4(a.out + (lp * P + row) * a.out_stride_bytes + j * 16, make_uint4(o[0], o[1], o[2], o[3]));
     }
 }
 

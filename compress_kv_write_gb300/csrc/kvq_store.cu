@@ -4,31 +4,29 @@
 // (section 1 store_row, and the store-latency table).
 //
 // Design (HBM-bound streaming, one pass):
-//  * Persistent CTAs, as many as are resident at once; CTA b owns the
-//    contiguous token range [n*b/G, n*(b+1)/G).
-//  * A producer warp streams each token's 512-value row (and, with RoPE,
-//    its 256-byte cos/sin row) into a ring of S shared-memory slots with 1-D
-//    bulk async copies that complete on the slot's "full" mbarrier.  Lane l
-//    owns slots l, l+32, ...; it prefetches the next token's slot index and
-//    position while the current copies are in flight.
-//  * Eight consumer warps take tokens round-robin.  A consumer reads its row
-//    out of the slot (lane l: 16-byte chunks l, l+32, ... -- conflict-free),
-//    frees the slot on its "empty" mbarrier, then computes in registers and
-//    writes the codes with coalesced stores (every warp store instruction
-//    covers one contiguous span of the code row) and the scale row with one
-//    16-byte store.
-//  * A 32-value quant block is LPB = 32 / (values per chunk) adjacent lanes
-//    (4 for bf16 rows, 8 for fp32); its absmax is a max of |x| over the
-//    lane's values and an xor-shuffle over those lanes.
-//  * Every mbarrier wait is bounded (2 s); a wait that runs out sets
-//    KVQ_DEVERR_TIMEOUT and the warp stops.
+//  * Persistent CTAs of four warps, as many as are resident at once; warp w
+//    of W owns the contiguous token range [n*w/W, n*(w+1)/W).
+//  * Each warp keeps D tokens in flight: every lane copies its own 16-byte
+//    chunks of the next rows (and, with RoPE, its own cos/sin values) into a
+//    per-warp shared-memory ring with cp.async, one commit group per token,
+//    and reads back only what it copied itself -- no cross-lane waits.  The
+//    loads cost no registers, so D rows per warp are in flight while the
+//    warp computes.
+//  * Slot indices and positions of 32 tokens at a time sit one per lane and
+//    are fetched with a shuffle when a token is issued or stored.
+//  * Lane l owns the chunks l, l+32, ... of a row, so every warp-wide load
+//    and store instruction covers one contiguous span.  A 32-value quant
+//    block is LPB = 32 / (values per chunk) adjacent lanes (4 for bf16 rows,
+//    8 for fp32); its absmax is a max of |x| over the lane's values and an
+//    xor-shuffle over those lanes, and the block's leading lane writes its
+//    scale byte.
 #include "kvq_launch.cuh"
 
 namespace kvq {
 namespace {
 
-constexpr int kConsumers = 8;
-constexpr int kStoreThreads = (kConsumers + 1) * 32;
+constexpr int kStoreWarps = 4;
+constexpr int kStoreThreads = kStoreWarps * 32;
 
 struct StoreArgs {
     const uint8_t *x;
@@ -47,19 +45,14 @@ struct StoreArgs {
 
 template <bool kBf16, bool kRope>
 struct StoreSmem {
-    static constexpr int XB = kD * (kBf16 ? 2 : 4);   // input row bytes
-    static constexpr int CSB = kRope ? kRopeD * 4 : 0;  // cos/sin row bytes
-    static constexpr int S = kBf16 ? 64 : 32;          // ring slots
-    static_assert(S % 32 == 0, "each producer lane owns whole slots");
-    static constexpr int kX = 0;
-    static constexpr int kCs = kX + S * XB;
-    static constexpr int kLoc = kCs + S * CSB;
-    static constexpr int kFlag = kLoc + S * 8;
-    static constexpr int kFull = kFlag + S * 4;
-    static constexpr int kEmpty = kFull + S * 8;
-    static constexpr int kScale = kEmpty + S * 8;
-    static constexpr int kBytes = kScale + kConsumers * kNBlk;
-    static_assert(kCs % 16 == 0 && kLoc % 16 == 0 && kFull % 8 == 0, "aligned smem regions");
+    static constexpr int XB = kD * (kBf16 ? 2 : 4);    // input row bytes
+    static constexpr int CSB = kRope ? kRopeD * 4 : 0;  // this token's cos/sin values
+    static constexpr int D = kBf16 ? 4 : 3;             // tokens in flight per warp
+    static constexpr int NS = D + 1;                    // ring slots per warp
+    static constexpr int SLOT = XB + CSB;
+    static constexpr int kWarpBytes = NS * SLOT;
+    static constexpr int kBytes = kStoreWarps * kWarpBytes;
+    static_assert(SLOT % 16 == 0 && kWarpBytes % 16 == 0, "16-byte aligned slots");
 };
 
 template <bool kBf16>
@@ -79,24 +72,33 @@ __device__ __forceinline__ void unpack_chunk(const uint4 &r, float *v) {
     }
 }
 
-// Quantise one token held as v[K][E] (lane's chunks k*32 + lane) and write it.
+// Quantise one token held as v[K][E] (lane's chunks k*32 + lane) and write
+// its code row and scale row into slot `slot` (validated, < 2^31).  The lane
+// that leads a quant block writes that block's scale byte.
 template <Layout L, int PageBits, int E, int K>
-__device__ __forceinline__ void encode_store(float (&v)[K][E], int64_t slot, uint8_t *pool,
-                                             uint8_t *scale_scratch, int lane) {
+__device__ __forceinline__ void encode_store(float (&v)[K][E], int32_t slot, uint8_t *pool, int lane) {
     constexpr int LPB = kBlock / E;
     using PK = PagedKV<L, PageBits>;
     using T = LayoutTraits<L>;
     float am[K];
 #pragma unroll
     for (int k = 0; k < K; ++k) {
-        float m = 0.f;
+        float m[E / 2];
 #pragma unroll
-        for (int e = 0; e < E; ++e) m = fmaxf(m, fabsf(v[k][e]));
+        for (int e = 0; e < E / 2; ++e) m[e] = fmaxf(fabsf(v[k][2 * e]), fabsf(v[k][2 * e + 1]));
 #pragma unroll
-        for (int off = 1; off < LPB; off <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-        am[k] = m;
+        for (int w = E / 4; w >= 1; w >>= 1)
+#pragma unroll
+            for (int e = 0; e < w; ++e) m[e] = fmaxf(m[e], m[e + w]);
+        float mm = m[0];
+#pragma unroll
+        for (int off = 1; off < LPB; off <<= 1) mm = fmaxf(mm, __shfl_xor_sync(0xffffffffu, mm, off));
+        am[k] = mm;
     }
-    uint8_t *crow = PK::code_row(pool, slot);
+    const int64_t page = int64_t(slot >> PageBits) * PK::kPageBytes;
+    const int row = slot & int(PK::kPage - 1);
+    uint8_t *crow = pool + page + row * T::kCodeBytes;
+    uint8_t *srow = pool + page + PK::kPage * T::kCodeBytes + row * T::kScaleBytes;
 #pragma unroll
     for (int k = 0; k < K; ++k) {
         const int c = k * 32 + lane;  // chunk index in the row
@@ -134,103 +136,86 @@ __device__ __forceinline__ void encode_store(float (&v)[K][E], int64_t slot, uin
                 *reinterpret_cast<uint16_t *>(crow + c * 2) = uint16_t(word);
             }
         }
-        if (lane % LPB == 0) scale_scratch[c / LPB] = uint8_t(sbyte);
+        if (lane % LPB == 0) srow[c / LPB] = uint8_t(sbyte);
     }
-    __syncwarp();
-    uint8_t *srow = PK::scale_row(pool, slot);
-    if (lane == 0) st_u4(srow, *reinterpret_cast<const uint4 *>(scale_scratch));
     if constexpr (T::kScaleBytes == 32) {
-        if (lane == 1) st_u4(srow + 16, make_uint4(0u, 0u, 0u, 0u));
+        if (lane == 0) st_u4(srow + 16, make_uint4(0u, 0u, 0u, 0u));
     }
-    __syncwarp();
 }
 
 template <Layout L, int PageBits, bool kBf16, bool kLoc64, bool kNorm, bool kRope>
-__global__ void __launch_bounds__(kStoreThreads, 2) store_kernel(const StoreArgs a) {
+__global__ void __launch_bounds__(kStoreThreads) store_kernel(const StoreArgs a) {
     using SM = StoreSmem<kBf16, kRope>;
-    constexpr int S = SM::S;
+    constexpr int D = SM::D, NS = SM::NS;
     constexpr int E = kBf16 ? 8 : 4;          // values per 16-byte chunk
     constexpr int K = kD / E / 32;            // chunks per lane
     constexpr int kRopeLane0 = kRopeStart / E - (K - 1) * 32;  // first rope lane of chunk K-1
     static_assert(kRopeLane0 >= 0 && kRopeLane0 < 32, "rope dims sit in the last chunk");
+    static_assert((32 - kRopeLane0) * E * 4 == SM::CSB || !kRope, "rope lanes fill the cos/sin area");
+    static_assert(D < 32, "a token's slot index is in the current or the next batch of 32");
 
-    extern __shared__ __align__(128) uint8_t smem[];
-    uint8_t *s_x = smem + SM::kX;
-    float *s_cs = reinterpret_cast<float *>(smem + SM::kCs);
-    int64_t *s_loc = reinterpret_cast<int64_t *>(smem + SM::kLoc);
-    int32_t *s_flag = reinterpret_cast<int32_t *>(smem + SM::kFlag);
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + SM::kFull);
-    uint64_t *empty = reinterpret_cast<uint64_t *>(smem + SM::kEmpty);
-    uint8_t *s_scale = smem + SM::kScale;
-
+    extern __shared__ __align__(16) uint8_t smem[];
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int64_t G = gridDim.x;
-    const int64_t start = a.n * int64_t(blockIdx.x) / G;
-    const int cnt = int(a.n * (int64_t(blockIdx.x) + 1) / G - start);
+    uint8_t *wsm = smem + warp * SM::kWarpBytes;
+    const int64_t W = int64_t(gridDim.x) * kStoreWarps;
+    const int64_t gw = int64_t(blockIdx.x) * kStoreWarps + warp;
+    const int64_t start = a.n * gw / W;
+    const int cnt = int(a.n * (gw + 1) / W - start);
 
-    if (threadIdx.x < S) {
-        mbar_init(&full[threadIdx.x], 1);
-        mbar_init(&empty[threadIdx.x], 1);
-    }
-    fence_mbar_init();
-    __syncthreads();
     pdl_wait();
 
-    if (warp == kConsumers) {
-        // ------------------------------------------------------------ producer
-        int64_t lc = 0;
-        int32_t p = 0;
-        if (lane < cnt) {
-            lc = kLoc64 ? __ldg(static_cast<const int64_t *>(a.loc) + start + lane)
-                        : int64_t(__ldg(static_cast<const int32_t *>(a.loc) + start + lane));
-            if constexpr (kRope) p = __ldg(a.pos + start + lane);
-        }
-        bool ok = true;
-        int i = lane;
-        for (; i < cnt; i += 32) {
-            const int64_t lc_cur = lc;
-            const int32_t p_cur = p;
-            if (i + 32 < cnt) {  // prefetch the next token's slot index and position
-                lc = kLoc64 ? __ldg(static_cast<const int64_t *>(a.loc) + start + i + 32)
-                            : int64_t(__ldg(static_cast<const int32_t *>(a.loc) + start + i + 32));
-                if constexpr (kRope) p = __ldg(a.pos + start + i + 32);
-            }
-            const int s = i % S;
-            const uint32_t r = uint32_t(i / S);
-            if (r > 0 && !mbar_wait(&empty[s], (r - 1) & 1u)) {
-                raise_err(a.err, KVQ_DEVERR_TIMEOUT);
-                ok = false;
-                break;
-            }
-            mbar_expect_tx(&full[s], SM::XB);
-            bulk_g2s(s_x + s * SM::XB, a.x + (start + i) * a.row_stride_bytes, SM::XB, &full[s]);
-            int32_t flag = 0;
+    // Slot / position of tokens 32b .. 32b+31 of this warp, one per lane,
+    // validated once: an out-of-range slot or position becomes -1.
+    auto ld_slot = [&](int j) -> int32_t {
+        const int64_t s = kLoc64 ? __ldg(static_cast<const int64_t *>(a.loc) + start + j)
+                                 : int64_t(__ldg(static_cast<const int32_t *>(a.loc) + start + j));
+        return (s >= 0 && s < a.pool_slots) ? int32_t(s) : -1;
+    };
+    auto ld_pos = [&](int j) -> int32_t {
+        const int32_t p = __ldg(a.pos + start + j);
+        return (p >= 0 && int64_t(p) < a.cs_rows) ? p : -1;
+    };
+    int32_t sl_cur = -1, sl_nxt = -1, p_cur = -1, p_nxt = -1;
+    if (lane < cnt) {
+        sl_cur = ld_slot(lane);
+        if constexpr (kRope) p_cur = ld_pos(lane);
+    }
+    if (32 + lane < cnt) {
+        sl_nxt = ld_slot(32 + lane);
+        if constexpr (kRope) p_nxt = ld_pos(32 + lane);
+    }
+    int cur_b = 0;
+
+    // copies of token j into the next ring slot; one commit group per token
+    const uint8_t *src_next = a.x + start * a.row_stride_bytes + lane * 16;
+    int ring_in = 0;
+    auto issue = [&](int j) {
+        if (j < cnt) {
+            uint8_t *slot = wsm + ring_in * SM::SLOT + lane * 16;
+#pragma unroll
+            for (int k = 0; k < K; ++k) cp_async16(slot + k * 512, src_next + k * 512);
             if constexpr (kRope) {
-                if (p_cur >= 0 && int64_t(p_cur) < a.cs_rows) {
-                    mbar_expect_tx(&full[s], SM::CSB);
-                    bulk_g2s(s_cs + s * kRopeD, a.cs + int64_t(p_cur) * kRopeD, SM::CSB, &full[s]);
-                } else {
-                    flag = 1;
+                const int32_t pj = __shfl_sync(0xffffffffu, (j >> 5) == cur_b ? p_cur : p_nxt, j & 31);
+                if (lane >= kRopeLane0 && pj >= 0) {
+                    const int i0 = ((K - 1) * 32 + lane) * E / 2 - kRopeStart / 2;
+                    const float *cs = a.cs + int64_t(pj) * kRopeD;
+                    uint8_t *dst = wsm + ring_in * SM::SLOT + SM::XB + (lane - kRopeLane0) * E * 4;
+                    if constexpr (E == 8) {
+                        cp_async16(dst, cs + i0);
+                        cp_async16(dst + 16, cs + kRopeD / 2 + i0);
+                    } else {
+                        cp_async8(dst, cs + i0);
+                        cp_async8(dst + 8, cs + kRopeD / 2 + i0);
+                    }
                 }
             }
-            s_loc[s] = lc_cur;
-            s_flag[s] = flag;
-            mbar_arrive(&full[s]);
+            src_next += a.row_stride_bytes;
+            ring_in = ring_in == NS - 1 ? 0 : ring_in + 1;
         }
-        pdl_trigger();
-        // drain: the last copies issued into this lane's slots have landed
-        // before the CTA (and its shared memory) can go away
-        for (int j = i - 32; j >= 0 && j >= i - S; j -= 32) {
-            if (!mbar_wait(&full[j % S], uint32_t(j / S) & 1u)) {
-                if (ok) raise_err(a.err, KVQ_DEVERR_TIMEOUT);
-                break;
-            }
-        }
-        return;
-    }
+        cp_async_commit();
+    };
 
-    // ---------------------------------------------------------------- consumers
     float wreg[K][E];
     if constexpr (kNorm) {
 #pragma unroll
@@ -246,71 +231,79 @@ __global__ void __launch_bounds__(kStoreThreads, 2) store_kernel(const StoreArgs
             }
         }
     }
-    uint8_t *scratch = s_scale + warp * kNBlk;
 
-    for (int i = warp; i < cnt; i += kConsumers) {
-        const int s = i % S;
-        const bool got = mbar_wait(&full[s], uint32_t(i / S) & 1u);
-        if (!__all_sync(0xffffffffu, got)) {
-            if (lane == 0) raise_err(a.err, KVQ_DEVERR_TIMEOUT);
-            break;
-        }
-        uint4 raw[K];
-        const uint8_t *xs = s_x + s * SM::XB;
 #pragma unroll
-        for (int k = 0; k < K; ++k) raw[k] = lds_u4(xs + (k * 32 + lane) * 16);
+    for (int j = 0; j < D; ++j) issue(j);
+    pdl_trigger();
+
+    int ring_out = 0;
+    for (int k = 0; k < cnt; ++k) {
+        if ((k & 31) == 0 && k > 0) {  // next batch of slots / positions
+            sl_cur = sl_nxt;
+            p_cur = p_nxt;
+            cur_b = k >> 5;
+            if (k + 32 + lane < cnt) {
+                sl_nxt = ld_slot(k + 32 + lane);
+                if constexpr (kRope) p_nxt = ld_pos(k + 32 + lane);
+            }
+        }
+        cp_async_wait<D - 1>();  // this lane's copies of token k have landed
+        const uint8_t *slot_sm = wsm + ring_out * SM::SLOT;
+        ring_out = ring_out == NS - 1 ? 0 : ring_out + 1;
+        uint4 raw[K];
+#pragma unroll
+        for (int kk = 0; kk < K; ++kk) raw[kk] = lds_u4(slot_sm + (kk * 32 + lane) * 16);
         float cosv[E / 2], sinv[E / 2];
         if constexpr (kRope) {
             if (lane >= kRopeLane0) {
-                const int i0 = ((K - 1) * 32 + lane) * E / 2 - kRopeStart / 2;
-                const float *cs = s_cs + s * kRopeD;
+                const float *cs = reinterpret_cast<const float *>(slot_sm + SM::XB + (lane - kRopeLane0) * E * 4);
 #pragma unroll
                 for (int q = 0; q < E / 2; ++q) {
-                    cosv[q] = cs[i0 + q];
-                    sinv[q] = cs[kRopeD / 2 + i0 + q];
+                    cosv[q] = cs[q];
+                    sinv[q] = cs[E / 2 + q];
                 }
             }
         }
-        const int64_t slot = s_loc[s];
-        const int32_t flag = s_flag[s];
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);  // the slot is free again
+        const int32_t slot = __shfl_sync(0xffffffffu, sl_cur, k & 31);
+        int32_t pk = 0;
+        if constexpr (kRope) pk = __shfl_sync(0xffffffffu, p_cur, k & 31);
+        issue(k + D);  // refill the ring while this token is computed
 
-        if (flag) {
+        if (kRope && pk < 0) {
             if (lane == 0) raise_err(a.err, KVQ_DEVERR_POS);
             continue;
         }
-        if (slot < 0 || slot >= a.pool_slots) {
+        if (slot < 0) {
             if (lane == 0) raise_err(a.err, KVQ_DEVERR_SLOT);
             continue;
         }
 
         float v[K][E];
 #pragma unroll
-        for (int k = 0; k < K; ++k) unpack_chunk<kBf16>(raw[k], v[k]);
+        for (int kk = 0; kk < K; ++kk) unpack_chunk<kBf16>(raw[kk], v[kk]);
 
         if constexpr (kNorm) {
             float2 ss2 = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int k = 0; k < K; ++k)
+            for (int kk = 0; kk < K; ++kk)
 #pragma unroll
                 for (int e = 0; e < E; e += 2) {
-                    const float2 t = make_float2(v[k][e], v[k][e + 1]);
+                    const float2 t = make_float2(v[kk][e], v[kk][e + 1]);
                     ss2 = ffma2(t, t, ss2);
                 }
             float ss = ss2.x + ss2.y;
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
             const float ms = ss * (1.0f / kD);
-            const float inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, a.eps)));
+            const float inv = rsqrt_approx(__fadd_rn(ms, a.eps));
 #pragma unroll
-            for (int k = 0; k < K; ++k)
+            for (int kk = 0; kk < K; ++kk)
 #pragma unroll
                 for (int e = 0; e < E; e += 2) {
-                    float2 t = fmul2(make_float2(v[k][e], v[k][e + 1]), make_float2(inv, inv));
-                    t = fmul2(t, make_float2(wreg[k][e], wreg[k][e + 1]));
-                    v[k][e] = t.x;
-                    v[k][e + 1] = t.y;
+                    float2 t = fmul2(make_float2(v[kk][e], v[kk][e + 1]), make_float2(inv, inv));
+                    t = fmul2(t, make_float2(wreg[kk][e], wreg[kk][e + 1]));
+                    v[kk][e] = t.x;
+                    v[kk][e + 1] = t.y;
                 }
         }
         if constexpr (kRope) {
@@ -326,16 +319,17 @@ __global__ void __launch_bounds__(kStoreThreads, 2) store_kernel(const StoreArgs
         }
         if constexpr (kNorm || kRope) {
 #pragma unroll
-            for (int k = 0; k < K; ++k)
+            for (int kk = 0; kk < K; ++kk)
 #pragma unroll
                 for (int e = 0; e < E; e += 2) {
-                    const uint32_t b = pack_bf16x2(v[k][e], v[k][e + 1]);
-                    v[k][e] = bf16_lo(b);
-                    v[k][e + 1] = bf16_hi(b);
+                    const uint32_t b = pack_bf16x2(v[kk][e], v[kk][e + 1]);
+                    v[kk][e] = bf16_lo(b);
+                    v[kk][e + 1] = bf16_hi(b);
                 }
         }
-        encode_store<L, PageBits, E, K>(v, slot, a.pool, scratch, lane);
+        encode_store<L, PageBits, E, K>(v, slot, a.pool, lane);
     }
+    cp_async_wait<0>();
 }
 
 template <Layout L, int PB, bool B16, bool L64, bool N, bool R>
@@ -345,7 +339,8 @@ kvq_status launch_store(const StoreArgs &a, cudaStream_t stream) {
     int64_t cap = 0;
     kvq_status st = resident_grid<kern>(kStoreThreads, smem, &cap);
     if (st != KVQ_OK) return st;
-    const int64_t grid = a.n < cap ? a.n : cap;
+    const int64_t want = (a.n + kStoreWarps - 1) / kStoreWarps;
+    const int64_t grid = want < cap ? want : cap;
     return launch_pdl_smem(kern, dim3(unsigned(grid)), dim3(kStoreThreads), smem, stream, a);
 }
 
@@ -362,6 +357,7 @@ extern "C" kvq_status kvq_store(kvq_layout layout, int page_bits, unsigned flags
                                 struct CUstream_st *stream) {
     kvq_status st = check_pool(layout, page_bits, pool, pool_slots);
     if (st != KVQ_OK) return st;
+    if (pool_slots > 0x7FFFFFFF) return KVQ_ERR_INVALID_ARG;  // slots are held as int32
     if (flags & ~unsigned(KVQ_FLAG_ROPE | KVQ_FLAG_NORM)) return KVQ_ERR_INVALID_ARG;
     if (x_dtype != KVQ_F32 && x_dtype != KVQ_BF16) return KVQ_ERR_INVALID_ARG;
     if (loc_dtype != KVQ_I32 && loc_dtype != KVQ_I64) return KVQ_ERR_INVALID_ARG;
