@@ -421,15 +421,19 @@ def measured_hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+KERNEL_SOURCES = {"store": "kvq_store.cu", "dequant": "kvq_dequant.cu", "compress": "kvq_compress.cu"}
+
+
 def traffic_from_profiles(workload):
-    """DRAM bytes per launch of the dominant kernel from the committed ncu
-    summary, if the kernel sources are unchanged since it was taken."""
+    """DRAM bytes per launch of the dominant kernel, from the committed ncu
+    summary (profiles/traffic.txt), if that kernel's sources are unchanged
+    since the counters were taken; else None."""
     path = os.path.join(ROOT, "profiles", "traffic.txt")
     try:
         lines = open(path).read().splitlines()
     except OSError:
         return None
-    sha = kernel_source_sha()
+    sha = kernel_source_sha(workload)
     for ln in lines:
         p = ln.split()
         if len(p) >= 4 and not ln.startswith("#") and p[0] == workload and p[3] == sha:
@@ -437,11 +441,13 @@ def traffic_from_profiles(workload):
     return None
 
 
-def kernel_source_sha():
+def kernel_source_sha(workload):
+    """Hash of the dominant kernel's translation unit and the shared headers."""
     import hashlib
     h = hashlib.sha256()
     d = os.path.join(ROOT, "compress_kv_write_gb300", "csrc")
-    for fn in sorted(os.listdir(d)):
+    files = [KERNEL_SOURCES[SPECS[workload]["kind"]], "kvq_device.cuh", "kvq_launch.cuh"]
+    for fn in files:
         with open(os.path.join(d, fn), "rb") as f:
             h.update(fn.encode())
             h.update(f.read())

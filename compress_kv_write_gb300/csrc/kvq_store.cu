@@ -3,23 +3,24 @@
 // kernels of "[sglang] DeepSeek V4.1 Paged KV Cache: V41 and FP4 formats"
 // (section 1 store_row, and the store-latency table).
 //
-// Design (HBM-bound streaming, one pass):
-//  * Persistent CTAs of four warps, as many as are resident at once; warp w
-//    of W owns the contiguous token range [n*w/W, n*(w+1)/W).
-//  * Each warp keeps D tokens in flight: every lane copies its own 16-byte
-//    chunks of the next rows (and, with RoPE, its own cos/sin values) into a
-//    per-warp shared-memory ring with cp.async, one commit group per token,
-//    and reads back only what it copied itself -- no cross-lane waits.  The
-//    loads cost no registers, so D rows per warp are in flight while the
-//    warp computes.
-//  * Slot indices and positions of 32 tokens at a time sit one per lane and
-//    are fetched with a shuffle when a token is issued or stored.
-//  * Lane l owns the chunks l, l+32, ... of a row, so every warp-wide load
-//    and store instruction covers one contiguous span.  A 32-value quant
-//    block is LPB = 32 / (values per chunk) adjacent lanes (4 for bf16 rows,
-//    8 for fp32); its absmax is a max of |x| over the lane's values and an
-//    xor-shuffle over those lanes, and the block's leading lane writes its
-//    scale byte.
+// Both kernels are persistent (as many CTAs of four warps as are resident at
+// once); warp w of W owns the contiguous token range [n*w/W, n*(w+1)/W) and
+// keeps its next rows in flight in a per-warp shared-memory ring filled with
+// cp.async (one commit group per ring slot).  Slot indices and positions of
+// 32 tokens sit one per lane, validated once, and are fetched with a
+// shuffle.  Math is fp32; the products of the RMSNorm and of the rotation are
+// rounded one by one, as in the definition.
+//
+//  * store_warp_kernel (V41): one warp per token.  Lane l owns the 16-byte
+//    chunks l, l+32, ... of the row, so every warp load / store instruction
+//    covers one contiguous span; a 32-value quant block is 32/(values per
+//    chunk) adjacent lanes, reduced with xor shuffles.  Each lane copies and
+//    reads back only its own chunks: no cross-lane waits.
+//  * store_pair_kernel (V41_FP4): two tokens per warp; half-warp h holds
+//    token 2k+h and lane i of the half owns quant block i.  The block
+//    absmax needs no shuffle and each block's e4m3 scale and reciprocal are
+//    computed once.  Rows land block-swizzled in shared memory so the
+//    block-per-lane reads are bank-conflict-free.
 #include "kvq_launch.cuh"
 
 namespace kvq {
@@ -43,17 +44,14 @@ struct StoreArgs {
     int32_t *err;
 };
 
-template <bool kBf16, bool kRope>
-struct StoreSmem {
-    static constexpr int XB = kD * (kBf16 ? 2 : 4);    // input row bytes
-    static constexpr int CSB = kRope ? kRopeD * 4 : 0;  // this token's cos/sin values
-    static constexpr int D = kBf16 ? 4 : 3;             // tokens in flight per warp
-    static constexpr int NS = D + 1;                    // ring slots per warp
-    static constexpr int SLOT = XB + CSB;
-    static constexpr int kWarpBytes = NS * SLOT;
-    static constexpr int kBytes = kStoreWarps * kWarpBytes;
-    static_assert(SLOT % 16 == 0 && kWarpBytes % 16 == 0, "16-byte aligned slots");
-};
+// 16-byte chunk position of (block, sub-chunk) inside a row: the sub-chunks
+// of a block are rotated so that eight lanes reading sub-chunk j of eight
+// consecutive blocks hit eight different bank groups.
+template <int SUBS>
+__device__ __forceinline__ int swz(int blk, int sub) {
+    const int rot = SUBS == 4 ? (blk >> 1) : blk;
+    return blk * SUBS + ((sub + rot) & (SUBS - 1));
+}
 
 template <bool kBf16>
 __device__ __forceinline__ void unpack_chunk(const uint4 &r, float *v) {
@@ -71,6 +69,18 @@ __device__ __forceinline__ void unpack_chunk(const uint4 &r, float *v) {
         v[3] = __uint_as_float(r.w);
     }
 }
+
+template <bool kBf16, bool kRope>
+struct WarpStoreSmem {
+    static constexpr int XB = kD * (kBf16 ? 2 : 4);    // input row bytes
+    static constexpr int CSB = kRope ? kRopeD * 4 : 0;  // this token's cos/sin values
+    static constexpr int D = kBf16 ? 4 : 3;             // tokens in flight per warp
+    static constexpr int NS = D + 1;                    // ring slots per warp
+    static constexpr int SLOT = XB + CSB;
+    static constexpr int kWarpBytes = NS * SLOT;
+    static constexpr int kBytes = kStoreWarps * kWarpBytes;
+    static_assert(SLOT % 16 == 0 && kWarpBytes % 16 == 0, "16-byte aligned slots");
+};
 
 // Quantise one token held as v[K][E] (lane's chunks k*32 + lane) and write
 // its code row and scale row into slot `slot` (validated, < 2^31).  The lane
@@ -144,8 +154,8 @@ __device__ __forceinline__ void encode_store(float (&v)[K][E], int32_t slot, uin
 }
 
 template <Layout L, int PageBits, bool kBf16, bool kLoc64, bool kNorm, bool kRope>
-__global__ void __launch_bounds__(kStoreThreads) store_kernel(const StoreArgs a) {
-    using SM = StoreSmem<kBf16, kRope>;
+__global__ void __launch_bounds__(kStoreThreads) store_warp_kernel(const StoreArgs a) {
+    using SM = WarpStoreSmem<kBf16, kRope>;
     constexpr int D = SM::D, NS = SM::NS;
     constexpr int E = kBf16 ? 8 : 4;          // values per 16-byte chunk
     constexpr int K = kD / E / 32;            // chunks per lane
@@ -332,16 +342,267 @@ __global__ void __launch_bounds__(kStoreThreads) store_kernel(const StoreArgs a)
     cp_async_wait<0>();
 }
 
+template <bool kBf16, bool kRope, bool kNorm>
+struct PairStoreSmem {
+    static constexpr int E = kBf16 ? 8 : 4;             // values per 16-byte chunk
+    static constexpr int SUBS = kBlock / E;             // chunks per quant block
+    static constexpr int CPR = kD / E;                  // chunks per row
+    static constexpr int XB = kD * (kBf16 ? 2 : 4);     // row bytes
+    static constexpr int CSB = kRope ? kRopeD * 4 : 0;  // cos/sin row bytes
+    static constexpr int D = kBf16 ? 2 : 1;             // token pairs in flight per warp
+    static constexpr int NS = D + 1;                    // ring slots per warp
+    static constexpr int SLOT = 2 * XB + 2 * CSB;
+    static constexpr int kWarpBytes = NS * SLOT;
+    static constexpr int kW = kStoreWarps * kWarpBytes;  // norm weights, swizzled
+    static constexpr int kBytes = kW + (kNorm ? kD * 4 : 0);
+    static_assert(SLOT % 16 == 0, "16-byte aligned slots");
+    static_assert((2 * CPR) % 32 == 0, "a pair is whole chunks per lane");
+};
+
+template <Layout L, int PageBits, bool kBf16, bool kLoc64, bool kNorm, bool kRope>
+__global__ void __launch_bounds__(kStoreThreads, 4) store_pair_kernel(const StoreArgs a) {
+    using SM = PairStoreSmem<kBf16, kRope, kNorm>;
+    using PK = PagedKV<L, PageBits>;
+    using T = LayoutTraits<L>;
+    constexpr int D = SM::D, NS = SM::NS, E = SM::E, SUBS = SM::SUBS, CPR = SM::CPR;
+    constexpr int NC = 2 * CPR / 32;          // chunks each lane copies per pair
+    constexpr int kRopeBlk0 = kRopeStart / kBlock;  // first rotated block (14)
+    static_assert(kRopeD == 2 * kBlock, "the rotated dims are the last two blocks");
+    static_assert(D < 16, "a pair's slot index is in the current or the next batch of 32");
+
+    extern __shared__ __align__(16) uint8_t smem[];
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int h = lane >> 4;   // token of the pair
+    const int bi = lane & 15;  // quant block owned
+    uint8_t *wsm = smem + warp * SM::kWarpBytes;
+    const float *s_w = reinterpret_cast<const float *>(smem + SM::kW);
+    const int64_t W = int64_t(gridDim.x) * kStoreWarps;
+    const int64_t gw = int64_t(blockIdx.x) * kStoreWarps + warp;
+    const int64_t start = a.n * gw / W;
+    const int cnt = int(a.n * (gw + 1) / W - start);
+    const int npairs = (cnt + 1) >> 1;
+
+    pdl_wait();
+
+    if constexpr (kNorm) {  // the weight row, block-swizzled like fp32 rows
+        float *w = reinterpret_cast<float *>(smem + SM::kW);
+        for (int c = threadIdx.x; c < kD / 4; c += kStoreThreads)
+            *reinterpret_cast<float4 *>(w + 4 * swz<8>(c >> 3, c & 7)) =
+                __ldg(reinterpret_cast<const float4 *>(a.w) + c);
+        __syncthreads();
+    }
+
+    // Slot / position of tokens 32b .. 32b+31 of this warp, one per lane,
+    // validated once: an out-of-range slot or position becomes -1.
+    auto ld_slot = [&](int j) -> int32_t {
+        const int64_t s = kLoc64 ? __ldg(static_cast<const int64_t *>(a.loc) + start + j)
+                                 : int64_t(__ldg(static_cast<const int32_t *>(a.loc) + start + j));
+        return (s >= 0 && s < a.pool_slots) ? int32_t(s) : -1;
+    };
+    auto ld_pos = [&](int j) -> int32_t {
+        const int32_t p = __ldg(a.pos + start + j);
+        return (p >= 0 && int64_t(p) < a.cs_rows) ? p : -1;
+    };
+    int32_t sl_cur = -1, sl_nxt = -1, p_cur = -1, p_nxt = -1;
+    if (lane < cnt) {
+        sl_cur = ld_slot(lane);
+        if constexpr (kRope) p_cur = ld_pos(lane);
+    }
+    if (32 + lane < cnt) {
+        sl_nxt = ld_slot(32 + lane);
+        if constexpr (kRope) p_nxt = ld_pos(32 + lane);
+    }
+    int cur_b = 0;
+
+    // copies of token pair p (tokens 2p, 2p+1) into the next ring slot
+    int ring_in = 0;
+    auto issue = [&](int p) {
+        if (p < npairs) {
+            uint8_t *slot = wsm + ring_in * SM::SLOT;
+#pragma unroll
+            for (int m = 0; m < NC; ++m) {
+                const int c = lane + 32 * m;
+                const int r = c / CPR, cc = c % CPR;
+                if (2 * p + r < cnt)
+                    cp_async16(slot + (r * CPR + swz<SUBS>(cc / SUBS, cc % SUBS)) * 16,
+                               a.x + (start + 2 * p + r) * a.row_stride_bytes + cc * 16);
+            }
+            if constexpr (kRope) {
+                const int t = 2 * p + h;
+                const int32_t pt = __shfl_sync(0xffffffffu, (t >> 5) == cur_b ? p_cur : p_nxt, t & 31);
+                if (t < cnt && pt >= 0)
+                    cp_async16(slot + 2 * SM::XB + h * SM::CSB + bi * 16, a.cs + int64_t(pt) * kRopeD + bi * 4);
+            }
+            ring_in = ring_in == NS - 1 ? 0 : ring_in + 1;
+        }
+        cp_async_commit();
+    };
+
+#pragma unroll
+    for (int p = 0; p < D; ++p) issue(p);
+    pdl_trigger();
+
+    int ring_out = 0;
+    for (int k = 0; k < npairs; ++k) {
+        if ((k & 15) == 0 && k > 0) {  // next batch of slots / positions
+            sl_cur = sl_nxt;
+            p_cur = p_nxt;
+            cur_b = k >> 4;
+            if (2 * k + 32 + lane < cnt) {
+                sl_nxt = ld_slot(2 * k + 32 + lane);
+                if constexpr (kRope) p_nxt = ld_pos(2 * k + 32 + lane);
+            }
+        }
+        cp_async_wait<D - 1>();  // this lane's copies of pair k have landed ...
+        __syncwarp();            // ... and so have the other lanes'
+        const uint8_t *slot_sm = wsm + ring_out * SM::SLOT;
+        ring_out = ring_out == NS - 1 ? 0 : ring_out + 1;
+
+        float v[kBlock];
+        {
+            const uint8_t *row = slot_sm + h * SM::XB;
+#pragma unroll
+            for (int j = 0; j < SUBS; ++j) unpack_chunk<kBf16>(lds_u4(row + swz<SUBS>(bi, j) * 16), v + j * E);
+        }
+        const int t = 2 * k + h;
+        const bool active = t < cnt;
+        const int32_t slot = __shfl_sync(0xffffffffu, sl_cur, t & 31);
+        int32_t pt = 0;
+        if constexpr (kRope) pt = __shfl_sync(0xffffffffu, p_cur, t & 31);
+
+        if constexpr (kNorm) {
+            float2 ss2 = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int e = 0; e < kBlock; e += 2) {
+                const float2 t2 = make_float2(v[e], v[e + 1]);
+                ss2 = ffma2(t2, t2, ss2);
+            }
+            float ss = ss2.x + ss2.y;
+#pragma unroll
+            for (int off = 8; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+            const float inv = rsqrt_approx(__fadd_rn(ss * (1.0f / kD), a.eps));
+            const float2 inv2 = make_float2(inv, inv);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float4 wv = *reinterpret_cast<const float4 *>(s_w + 4 * swz<8>(bi, j));
+                const float2 a0 = fmul2(fmul2(make_float2(v[4 * j], v[4 * j + 1]), inv2), make_float2(wv.x, wv.y));
+                const float2 a1 = fmul2(fmul2(make_float2(v[4 * j + 2], v[4 * j + 3]), inv2), make_float2(wv.z, wv.w));
+                v[4 * j] = a0.x;
+                v[4 * j + 1] = a0.y;
+                v[4 * j + 2] = a1.x;
+                v[4 * j + 3] = a1.y;
+            }
+        }
+        if constexpr (kRope) {
+            if (bi >= kRopeBlk0) {  // pairs (bi - 14) * 16 .. +15 of the rotation
+                const float *cs = reinterpret_cast<const float *>(slot_sm + 2 * SM::XB + h * SM::CSB);
+                const int q0 = (bi - kRopeBlk0) * (kBlock / 2);
+#pragma unroll
+                for (int g = 0; g < kBlock / 8; ++g) {
+                    const float4 c4 = *reinterpret_cast<const float4 *>(cs + q0 + 4 * g);
+                    const float4 s4 = *reinterpret_cast<const float4 *>(cs + kRopeD / 2 + q0 + 4 * g);
+                    const float cc[4] = {c4.x, c4.y, c4.z, c4.w}, sn[4] = {s4.x, s4.y, s4.z, s4.w};
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const float2 xv = make_float2(v[8 * g + 2 * q], v[8 * g + 2 * q + 1]);
+                        const float2 p = fmul2(xv, make_float2(cc[q], sn[q]));  // (a*c, b*s)
+                        const float2 r = fmul2(xv, make_float2(sn[q], cc[q]));  // (a*s, b*c)
+                        v[8 * g + 2 * q] = __fsub_rn(p.x, p.y);
+                        v[8 * g + 2 * q + 1] = __fadd_rn(r.x, r.y);
+                    }
+                }
+            }
+        }
+        issue(k + D);  // refill the ring while this pair is computed
+
+        if constexpr (kNorm || kRope) {
+#pragma unroll
+            for (int e = 0; e < kBlock; e += 2) {
+                const uint32_t b = pack_bf16x2(v[e], v[e + 1]);
+                v[e] = bf16_lo(b);
+                v[e + 1] = bf16_hi(b);
+            }
+        }
+        // block absmax (this lane holds the whole block): four running maxima
+        float m0 = fabsf(v[0]), m1 = fabsf(v[1]), m2 = fabsf(v[2]), m3 = fabsf(v[3]);
+#pragma unroll
+        for (int e = 4; e < kBlock; e += 4) {
+            m0 = fmaxf(m0, fabsf(v[e]));
+            m1 = fmaxf(m1, fabsf(v[e + 1]));
+            m2 = fmaxf(m2, fabsf(v[e + 2]));
+            m3 = fmaxf(m3, fabsf(v[e + 3]));
+        }
+        const uint32_t amax = __float_as_uint(fmaxf(fmaxf(m0, m1), fmaxf(m2, m3)));
+
+        const bool bad_pos = kRope && pt < 0;
+        if (!active || bad_pos || slot < 0) {
+            if (active && bi == 0) raise_err(a.err, bad_pos ? KVQ_DEVERR_POS : KVQ_DEVERR_SLOT);
+            continue;
+        }
+        const int64_t page = int64_t(slot >> PageBits) * PK::kPageBytes;
+        const int row = slot & int(PK::kPage - 1);
+        uint8_t *crow = a.pool + page + row * T::kCodeBytes;
+        uint8_t *srow = a.pool + page + PK::kPage * T::kCodeBytes + row * T::kScaleBytes;
+        uint32_t sbyte;
+        if constexpr (L == Layout::V41) {
+            sbyte = v41_scale_byte(amax);
+            const float mult = v41_multiplier(sbyte);
+            const float2 mult2 = make_float2(mult, mult);
+            uint32_t wd[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const float2 lo = fmul2(make_float2(v[4 * q], v[4 * q + 1]), mult2);
+                const float2 hi = fmul2(make_float2(v[4 * q + 2], v[4 * q + 3]), mult2);
+                wd[q] = cvt_e4m3x2(lo.x, lo.y) | (cvt_e4m3x2(hi.x, hi.y) << 16);
+            }
+            st_u4(crow + bi * 32, make_uint4(wd[0], wd[1], wd[2], wd[3]));
+            st_u4(crow + bi * 32 + 16, make_uint4(wd[4], wd[5], wd[6], wd[7]));
+        } else {
+            sbyte = fp4_scale_byte(amax);
+            const float S = e4m3x2_to_f32x2(sbyte).x;
+            const float inv = __frcp_rn(S);
+            uint32_t wd[4] = {0u, 0u, 0u, 0u};
+            if (S != 0.0f) {
+#pragma unroll
+                for (int q = 0; q < 16; ++q) {
+                    const float2 y = fmul2(make_float2(v[2 * q], v[2 * q + 1]), make_float2(inv, inv));
+                    wd[q >> 2] |= cvt_e2m1x2(y.x, y.y) << (8 * (q & 3));
+                }
+            }
+            st_u4(crow + bi * 16, make_uint4(wd[0], wd[1], wd[2], wd[3]));
+            if (bi == 0) st_u4(srow + 16, make_uint4(0u, 0u, 0u, 0u));
+        }
+        srow[bi] = uint8_t(sbyte);
+    }
+    cp_async_wait<0>();
+}
+
+// V41 rows use the warp-per-token kernel (fewer instructions for the
+// norm / RoPE paths); V41_FP4 rows use the pair kernel, which computes each
+// block's e4m3 scale and its reciprocal once per block instead of once per
+// lane of the block.
 template <Layout L, int PB, bool B16, bool L64, bool N, bool R>
 kvq_status launch_store(const StoreArgs &a, cudaStream_t stream) {
-    constexpr auto kern = store_kernel<L, PB, B16, L64, N, R>;
-    constexpr size_t smem = StoreSmem<B16, R>::kBytes;
-    int64_t cap = 0;
-    kvq_status st = resident_grid<kern>(kStoreThreads, smem, &cap);
-    if (st != KVQ_OK) return st;
-    const int64_t want = (a.n + kStoreWarps - 1) / kStoreWarps;
-    const int64_t grid = want < cap ? want : cap;
-    return launch_pdl_smem(kern, dim3(unsigned(grid)), dim3(kStoreThreads), smem, stream, a);
+    if constexpr (L == Layout::V41) {
+        constexpr auto kern = store_warp_kernel<L, PB, B16, L64, N, R>;
+        constexpr size_t smem = WarpStoreSmem<B16, R>::kBytes;
+        int64_t cap = 0;
+        kvq_status st = resident_grid<kern>(kStoreThreads, smem, &cap);
+        if (st != KVQ_OK) return st;
+        const int64_t want = (a.n + kStoreWarps - 1) / kStoreWarps;
+        const int64_t grid = want < cap ? want : cap;
+        return launch_pdl_smem(kern, dim3(unsigned(grid)), dim3(kStoreThreads), smem, stream, a);
+    } else {
+        constexpr auto kern = store_pair_kernel<L, PB, B16, L64, N, R>;
+        constexpr size_t smem = PairStoreSmem<B16, R, N>::kBytes;
+        int64_t cap = 0;
+        kvq_status st = resident_grid<kern>(kStoreThreads, smem, &cap);
+        if (st != KVQ_OK) return st;
+        const int64_t want = (a.n + 2 * kStoreWarps - 1) / (2 * kStoreWarps);
+        const int64_t grid = want < cap ? want : cap;
+        return launch_pdl_smem(kern, dim3(unsigned(grid)), dim3(kStoreThreads), smem, stream, a);
+    }
 }
 
 }  // namespace
