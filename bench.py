@@ -454,6 +454,18 @@ def kernel_source_sha(workload):
     return h.hexdigest()[:16]
 
 
+def max_over_ranks(value, device=None):
+    """The largest of every rank's value (the slowest rank's time); the value
+    itself when there is no process group of more than one rank."""
+    import torch
+    import torch.distributed as dist
+    if not dist.is_available() or not dist.is_initialized() or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device if device is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -549,10 +561,7 @@ def run_ours(args):
     clocks = sampler.stop() if (rank == 0 and not args.no_clocks) else None
     ms = e0.elapsed_time(e1)
     assert wl.err.item() == 0, "device error in the timed region"
-    if world > 1:
-        t = torch.tensor([ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, dev)
     ms_per_step = ms / K
     units_all = wl.units * K * world
     value = units_all / (ms / 1e3)
@@ -593,10 +602,7 @@ def run_ours(args):
             wl.e2e_step()
     stream.synchronize()
     e2e_s = time.perf_counter() - t0
-    if world > 1:
-        t = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t.item())
+    e2e_s = max_over_ranks(e2e_s, dev)
     e2e_value = wl.units * e2e_steps * world / e2e_s
 
     cpu = None
