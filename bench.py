@@ -49,6 +49,7 @@ def b_compress(r, payload=528):
 DEFAULT_STEPS = {
     "store_norm_rope": 200000, "store_rope": 200000, "store": 200000, "small": 200000,
     "fp4_store": 20000, "fp4_dequant": 3000, "c4a": 20000, "c128a": 1000, "c128a_fp4": 1000,
+    "layers": 2000, "dequant_select": 3000,
 }
 
 # the workloads: one per configuration of the write path
@@ -59,10 +60,16 @@ SPECS = {
     "store_norm_rope": dict(kind="store", flags=3, bs=16384, pool_slots=1 << 20, layout=1),
     "fp4_store": dict(kind="store", flags=0, bs=262144, pool_slots=1 << 21, layout=2, student_t=True),
     "fp4_dequant": dict(kind="dequant", pool_slots=1 << 21, layout=2),
+    # the consumer side: the rows a sparse attention selects, gathered by slot
+    "dequant_select": dict(kind="select", pool_slots=1 << 21, layout=2, n=1 << 18),
     "c4a": dict(kind="compress", ratio=4, layout=1, score_std=math.sqrt(2.0), groups=16384,
                 full_slots=1 << 20, swa_slots=1 << 17),
     "c128a": dict(kind="compress", ratio=128, layout=1, score_std=2.0, requests=256,
                   pool_slots=1 << 20),
+    # one decode step of a 61-layer model: the step's slots translated full -> SWA once, then
+    # every layer stores its K rows (norm + RoPE, V41) into its own SWA pool
+    "layers": dict(kind="layers", layers=61, bs=512, flags=3, layout=1, full_slots=1 << 20,
+                   swa_slots=1 << 17),
     "c128a_fp4": dict(kind="compress", ratio=128, layout=2, score_std=2.0, requests=256,
                       pool_slots=1 << 20),
 }
@@ -87,6 +94,15 @@ def describe(name):
         return {"workload": name, "layout": lay, "tokens": sp["pool_slots"], "page_size": 64,
                 "page_table": "random permutation of the pool's pages",
                 "rows": "0.5*Student-t(3) stored by the FP4 store"}, "tokens"
+    if sp["kind"] == "select":
+        return {"workload": name, "layout": lay, "pool_slots": sp["pool_slots"], "selected": sp["n"],
+                "slots": "random distinct int64 slots of the whole pool", "page_size": 64,
+                "rows": "0.5*Student-t(3) stored by the FP4 store"}, "tokens"
+    if sp["kind"] == "layers":
+        return {"workload": name, "layout": lay, "layers": sp["layers"], "bs": sp["bs"],
+                "flags": "norm+rope", "x_dtype": "bf16", "loc_dtype": "int64 full slots -> int32 SWA slots",
+                "full_slots": sp["full_slots"], "swa_slots_per_layer": sp["swa_slots"], "page_size": 64,
+                "translate": "once per step, shared by every layer"}, "KV tokens (tokens x layers)"
     cfg = {"workload": name, "layout": lay, "ratio": sp["ratio"], "page_size": 64,
            "values": "N(0,1) fp32", "scores": f"N(0,{sp['score_std'] ** 2:g}) fp32",
            "rope": "last 64 dims at the group's position"}
@@ -335,6 +351,124 @@ class CompressWorkload(Workload):
         self.herr.copy_(self.err, non_blocking=True)
 
 
+class SelectWorkload(Workload):
+    """Dequant of the rows a sparse attention selects from a full FP4 pool."""
+
+    def __init__(self, name, dev):
+        super().__init__(name, dev)
+        import torch
+        from compress_kv_write_gb300 import synth
+        sp = self.spec
+        self.layout, self.pool_slots, self.n = sp["layout"], sp["pool_slots"], sp["n"]
+        self.pool = torch.zeros(self.pool_slots * self.K.bytes_per_token(self.layout),
+                                dtype=torch.uint8, device=dev)
+        chunk = 1 << 18
+        x = synth.student_t_rows_bf16(chunk, dev, 0)
+        for c in range(self.pool_slots // chunk):
+            loc = torch.arange(c * chunk, (c + 1) * chunk, device=dev)
+            self.K.kvq_store(self.layout, 6, 0, x, loc, self.pool, self.pool_slots)
+        del x
+        self.R = 4
+        self.sel = [synth.injective_slots(self.n, self.pool_slots, dev, r) for r in range(self.R)]
+        self.out = torch.empty((self.n, 512), dtype=torch.bfloat16, device=dev)
+        self.units = self.n
+        payload = 528 if self.layout == 1 else 272
+        self.bytes_total = self.bytes_dominant = self.n * (payload + 1024 + 8)
+        self.dominant = "dequant_slots_kernel"
+        self.config["l2"] = (f"pool {self.pool_slots * 288 / 2**20:.0f} MB, random rows; output "
+                             f"{self.n * 1024 / 2**20:.0f} MB per step > 129 MB L2")
+
+    def step(self, i):
+        self.K.kvq_dequant_slots(self.layout, 6, self.pool, self.pool_slots, self.sel[i % self.R],
+                                 self.out, err=self.err)
+
+    def e2e_setup(self):
+        import torch
+        self.hsel = self.sel[0].cpu().pin_memory()
+        self.dsel = torch.empty_like(self.sel[0])
+        self.hout = torch.empty((self.n, 512), dtype=torch.bfloat16).pin_memory()
+        return self.hsel.numel() * 8, self.hout.numel() * 2
+
+    def e2e_step(self):
+        self.dsel.copy_(self.hsel, non_blocking=True)
+        self.K.kvq_dequant_slots(self.layout, 6, self.pool, self.pool_slots, self.dsel, self.out,
+                                 err=self.err)
+        self.hout.copy_(self.out, non_blocking=True)
+
+
+class LayersWorkload(Workload):
+    """One step of an L-layer model: translate the step's full-pool slots to SWA
+    slots once, then store each layer's K rows (norm + RoPE, V41) into that
+    layer's SWA pool with the shared translated slots."""
+
+    def __init__(self, name, dev):
+        super().__init__(name, dev)
+        import torch
+        from compress_kv_write_gb300 import synth
+        sp = self.spec
+        self.L, self.bs, self.flags = sp["layers"], sp["bs"], sp["flags"]
+        self.full_slots, self.swa_slots = sp["full_slots"], sp["swa_slots"]
+        per_set = self.L * self.bs * (1024 + 12)
+        self.R = _rotation(per_set, cap=8)
+        self.x, self.full_loc, self.table, self.pos = [], [], [], []
+        for r in range(self.R):
+            self.x.append([synth.store_rows_bf16(self.bs, dev, 1000 * r + l) for l in range(self.L)])
+            fl = synth.injective_slots(self.bs, self.full_slots, dev, r)
+            self.full_loc.append(fl)
+            self.table.append(synth.swa_table(self.full_slots, self.swa_slots, fl, dev, r))
+            self.pos.append(synth.positions(self.bs, dev, r))
+        self.cs = synth.rope_table(65536, dev)
+        self.w = [synth.norm_weight(dev, l) for l in range(self.L)]
+        self.pools = [torch.zeros(self.swa_slots * 528, dtype=torch.uint8, device=dev) for _ in range(self.L)]
+        self.swa_loc = torch.zeros(self.bs, dtype=torch.int32, device=dev)
+        self.launches = 1 + self.L
+        self.units = self.bs * self.L
+        per_store = self.bs * B_STORE_ROPE
+        self.bytes_dominant = per_store
+        self.bytes_total = self.L * per_store + self.bs * B_TRANSLATE
+        self.dominant = "store_kernel"
+        self.config["l2"] = (f"rotating {self.R} step input sets ({self.R * per_set / 2**20:.0f} MB) "
+                             f"over {self.L} pools of {self.swa_slots * 528 / 2**20:.0f} MB")
+
+    def _layer(self, r, l):
+        self.K.kvq_store(1, 6, self.flags, self.x[r][l], self.swa_loc, self.pools[l], self.swa_slots,
+                         norm_weight=self.w[l], eps=1e-6, cos_sin=self.cs, pos=self.pos[r], err=self.err)
+
+    def step(self, i):
+        r = i % self.R
+        self.K.kvq_translate_loc(self.full_loc[r], self.table[r], self.swa_loc, err=self.err)
+        for l in range(self.L):
+            self._layer(r, l)
+
+    def step_unhoisted(self, i):
+        """The same step with the translation repeated inside every layer."""
+        r = i % self.R
+        for l in range(self.L):
+            self.K.kvq_translate_loc(self.full_loc[r], self.table[r], self.swa_loc, err=self.err)
+            self._layer(r, l)
+
+    def dominant_step(self, i):
+        self._layer(i % self.R, i % self.L)
+
+    def e2e_setup(self):
+        import torch
+        self.hx = [x.cpu().pin_memory() for x in self.x[0]]
+        self.hloc = self.full_loc[0].cpu().pin_memory()
+        self.dx = [torch.empty_like(x) for x in self.x[0]]
+        self.dloc = torch.empty_like(self.full_loc[0])
+        self.herr = torch.zeros(1, dtype=torch.int32).pin_memory()
+        return sum(x.numel() * 2 for x in self.hx) + self.hloc.numel() * 8, 4
+
+    def e2e_step(self):
+        self.dloc.copy_(self.hloc, non_blocking=True)
+        self.K.kvq_translate_loc(self.dloc, self.table[0], self.swa_loc, err=self.err)
+        for l in range(self.L):
+            self.dx[l].copy_(self.hx[l], non_blocking=True)
+            self.K.kvq_store(1, 6, self.flags, self.dx[l], self.swa_loc, self.pools[l], self.swa_slots,
+                             norm_weight=self.w[l], eps=1e-6, cos_sin=self.cs, pos=self.pos[0], err=self.err)
+        self.herr.copy_(self.err, non_blocking=True)
+
+
 def make_workload(name, dev, tokens=None):
     """tokens (profiling only): shrink the workload to about this many KV tokens."""
     if tokens:
@@ -343,13 +477,18 @@ def make_workload(name, dev, tokens=None):
             sp["bs"] = int(tokens)
         elif sp["kind"] == "dequant":
             sp["pool_slots"] = max(1 << 18, (int(tokens) >> 18) << 18)
+        elif sp["kind"] == "layers":
+            sp["bs"] = max(1, int(tokens) // sp["layers"])
+        elif sp["kind"] == "select":
+            sp["n"] = int(tokens)
         elif sp["ratio"] == 4:
             sp["groups"] = max(1, int(tokens) // 4)
         else:
             sp["requests"] = max(1, int(tokens) * 256 // 1_500_000)
         SPECS[name] = sp
     kind = SPECS[name]["kind"]
-    cls = {"store": StoreWorkload, "dequant": DequantWorkload, "compress": CompressWorkload}[kind]
+    cls = {"store": StoreWorkload, "dequant": DequantWorkload, "compress": CompressWorkload,
+           "layers": LayersWorkload, "select": SelectWorkload}[kind]
     return cls(name, dev)
 
 
@@ -421,7 +560,8 @@ def measured_hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-KERNEL_SOURCES = {"store": "kvq_store.cu", "dequant": "kvq_dequant.cu", "compress": "kvq_compress.cu"}
+KERNEL_SOURCES = {"store": "kvq_store.cu", "dequant": "kvq_dequant.cu", "compress": "kvq_compress.cu",
+                  "layers": "kvq_store.cu", "select": "kvq_dequant.cu"}
 
 
 def traffic_from_profiles(workload):
@@ -583,6 +723,27 @@ def run_ours(args):
         dom_ms = d0.elapsed_time(d1) / nd
     else:
         dom_ms = ms_per_step
+    # the same step with the slot translation inside every layer (the un-hoisted form)
+    hoist = None
+    if hasattr(wl, "step_unhoisted"):
+        nu = min(K, chunk)
+        gu = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gu, stream=stream):
+            for i in range(nu):
+                wl.step_unhoisted(i)
+        with torch.cuda.stream(stream):
+            gu.replay()
+        torch.cuda.synchronize()
+        u0 = torch.cuda.Event(enable_timing=True)
+        u1 = torch.cuda.Event(enable_timing=True)
+        u0.record(stream)
+        with torch.cuda.stream(stream):
+            gu.replay()
+        u1.record(stream)
+        torch.cuda.synchronize()
+        un_ms = u0.elapsed_time(u1) / nu
+        hoist = {"hoisted_ms_per_step": ms_per_step, "translate_per_layer_ms_per_step": un_ms,
+                 "speedup": un_ms / ms_per_step, "layers": wl.L}
     peak, peak_src = measured_hbm_peak()
     achieved = wl.bytes_dominant / (dom_ms / 1e3) / 1e9
     step_gbs = wl.bytes_total / (ms_per_step / 1e3) / 1e9
@@ -624,6 +785,7 @@ def run_ours(args):
             "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": e2e_steps},
             "gpu_launches": wl.launches * K,
+            **({"hoist": hoist} if hoist else {}),
             "clocks": clocks,
             "cpu_baseline": cpu,
         }
@@ -640,7 +802,13 @@ def oracle_sample(name, n_rows):
     import oracle as O
     spec = SPECS[name]
     kind = spec["kind"]
-    if kind == "store":
+    if kind == "select":
+        n_pages = max(1, n_rows // 64)
+        x_np = synth.student_t_rows_bf16(n_pages * 64, "cpu", 0).view(torch.int16).numpy().view(np.uint16)
+        pool = np.zeros(n_pages * 64 * 288, np.uint8)
+        assert O.store(O.FP4, 6, 0, x_np, np.arange(n_pages * 64), pool) == O.OK
+        return dict(pool=pool, slots=np.random.default_rng(0).permutation(n_pages * 64))
+    if kind in ("store", "layers"):
         n = n_rows
         if spec.get("fp32"):
             x_np = synth.normal((n, 512), "cpu", 0, "x").numpy()
@@ -670,7 +838,12 @@ def oracle_run(name, smp, n_units):
     spec = SPECS[name]
     kind = spec["kind"]
     layout = spec.get("layout", 1)
-    if kind == "store":
+    if kind == "select":
+        n = max(1, min(n_units, smp["slots"].size))
+        rc, _ = O.dequant_slots(O.FP4, smp["pool"], smp["slots"][:n], 6)
+        assert rc == O.OK
+        return n
+    if kind in ("store", "layers"):
         n = min(n_units, smp["x"].shape[0])
         slots = max(64, -(-n // 64) * 64)
         pool = np.zeros(slots * O.bytes_per_token(layout), np.uint8)

@@ -76,14 +76,16 @@ kvq_status resident_grid(int threads, size_t smem, int64_t *grid_cap) {
     return KVQ_OK;
 }
 
-// page_bits values with compiled instances.
-inline bool page_bits_supported(int pb) { return pb == 2 || pb == 6; }
+// page_bits values with compiled instances: pages of 4, 16, 64 and 256 tokens.
+inline bool page_bits_supported(int pb) { return pb == 2 || pb == 4 || pb == 6 || pb == 8; }
 
 template <typename F>
 kvq_status with_page_bits(int pb, F &&f) {
     switch (pb) {
         case 2: return f(std::integral_constant<int, 2>{});
+        case 4: return f(std::integral_constant<int, 4>{});
         case 6: return f(std::integral_constant<int, 6>{});
+        case 8: return f(std::integral_constant<int, 8>{});
         default: return KVQ_ERR_UNSUPPORTED;
     }
 }

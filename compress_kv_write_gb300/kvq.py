@@ -45,6 +45,8 @@ _SIGS = {
     "kvq_compress": (C.c_int, [C.c_int, C.c_int, C.c_int, C.c_uint, C.c_void_p, C.c_void_p,
                                C.c_int64, C.c_void_p, C.c_int64, C.c_void_p, C.c_void_p,
                                C.c_void_p, C.c_int64, C.c_void_p, C.c_void_p]),
+    "kvq_dequant_slots": (C.c_int, [C.c_int, C.c_int, C.c_void_p, C.c_int64, C.c_void_p, C.c_int,
+                                    C.c_int64, C.c_void_p, C.c_int64, C.c_void_p, C.c_void_p]),
     "kvq_dequant": (C.c_int, [C.c_int, C.c_int, C.c_void_p, C.c_int64, C.c_void_p, C.c_int64,
                               C.c_void_p, C.c_int64, C.c_void_p, C.c_void_p]),
 }
@@ -230,3 +232,19 @@ def kvq_dequant(layout, page_bits, pool, pool_pages, page_table, out, err=None, 
     st = lib().kvq_dequant(layout, page_bits, _ptr(pool), int(pool_pages), _ptr(page_table),
                            n_tokens, _ptr(out), out.stride(0), _ptr(err), _stream(stream))
     _check(st, "kvq_dequant")
+
+
+def kvq_dequant_slots(layout, page_bits, pool, pool_slots, slots, out, err=None, stream=None):
+    """out [n, >=512] bf16 <- the tokens in slots [n] (int32/int64); slot -1 gives a zero row."""
+    _cuda(pool, "pool", (torch.uint8,))
+    _cuda(slots, "slots")
+    _cuda(out, "out", (torch.bfloat16,))
+    _contig1d(slots, "slots")
+    if out.dim() != 2 or out.shape[1] < HEAD_DIM or out.stride(1) != 1 or out.shape[0] != slots.numel():
+        raise ValueError("out must be [slots.numel(), >=512] bf16 with unit inner stride")
+    if pool.numel() < pool_slots * bytes_per_token(layout):
+        raise ValueError("pool is smaller than pool_slots tokens")
+    st = lib().kvq_dequant_slots(layout, page_bits, _ptr(pool), int(pool_slots), _ptr(slots),
+                                 _idx_dtype(slots, "slots"), slots.numel(), _ptr(out), out.stride(0),
+                                 _ptr(err), _stream(stream))
+    _check(st, "kvq_dequant_slots")

@@ -154,6 +154,20 @@ kvq_status kvq_dequant(kvq_layout layout, int page_bits,
                        void *out_bf16, int64_t out_row_stride,
                        int32_t *err, struct CUstream_st *stream);
 
+/* Dequant of selected tokens to bf16 rows: the consumer side of [P1] section
+ * 4 (dequant_k_cache.py) restricted to the tokens a sparse attention picks
+ * (the FlashMLA sparse-FP8 reader of [P3]).
+ *   slots       [n] int32 or int64 (slot_dtype): pool slot of output row i.
+ *   out_bf16    [n, out_row_stride] bf16 (stride >= 512, rows 16-B aligned):
+ *               row i = decode(slot slots[i]), exact in bf16 as in kvq_dequant.
+ * Slot -1 is padding and writes a zero row.  Any other slot outside
+ * [0, pool_slots) sets KVQ_DEVERR_SLOT and leaves row i untouched. */
+kvq_status kvq_dequant_slots(kvq_layout layout, int page_bits,
+                             const uint8_t *pool, int64_t pool_slots,
+                             const void *slots, kvq_index_dtype slot_dtype, int64_t n,
+                             void *out_bf16, int64_t out_row_stride,
+                             int32_t *err, struct CUstream_st *stream);
+
 /* Human-readable name of a status. */
 const char *kvq_status_string(kvq_status status);
 

@@ -26,6 +26,8 @@
  *                           address model; footprint closed forms
  *   or_dequant             pinned: dequant of hand-worked blocks, error bound,
  *                           page-table permutation brute force
+ *   or_dequant_slots       pinned: equals the paged dequant's rows (identity
+ *                           page table), padding and range rules
  *   or_translate           pinned: brute-force gather, zero tail, capacity rule
  */
 #include "kvq_oracle.h"
@@ -459,6 +461,22 @@ static uint16_t bf16_of_double(double v)
     return or_bf16_bits((float)v);
 }
 
+/* One token's 512 bf16 values from its code row and scale row. */
+static void decode_row(int layout, const uint8_t *codes, const uint8_t *scales, uint16_t *o)
+{
+    for (int d = 0; d < OR_D; ++d) {
+        double v;
+        if (layout == OR_V41) {
+            v = or_e4m3_decode(codes[d]) * ue8m0_value(scales[d / OR_BLOCK]);
+        } else {
+            uint8_t byte = codes[d / 2];
+            uint8_t nib = (d & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 0xFu);
+            v = or_e2m1_decode(nib) * or_e4m3_decode(scales[d / OR_BLOCK]);
+        }
+        o[d] = bf16_of_double(v);
+    }
+}
+
 int or_dequant(int layout, int page_bits, const uint8_t *pool, int64_t pool_pages,
                const int32_t *page_table, int64_t n_tokens,
                uint16_t *out_bf16, int64_t out_row_stride)
@@ -473,20 +491,32 @@ int or_dequant(int layout, int page_bits, const uint8_t *pool, int64_t pool_page
         int64_t phys = page_table[t >> page_bits];
         if (phys < 0 || phys >= pool_pages) { rc = OR_ERANGE; continue; }
         int64_t row = t & (P - 1);
-        const uint8_t *codes = pool + phys * PB + row * CB;
-        const uint8_t *scales = pool + phys * PB + P * CB + row * SB;
-        uint16_t *o = out_bf16 + t * out_row_stride;
-        for (int d = 0; d < OR_D; ++d) {
-            double v;
-            if (layout == OR_V41) {
-                v = or_e4m3_decode(codes[d]) * ue8m0_value(scales[d / OR_BLOCK]);
-            } else {
-                uint8_t byte = codes[d / 2];
-                uint8_t nib = (d & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 0xFu);
-                v = or_e2m1_decode(nib) * or_e4m3_decode(scales[d / OR_BLOCK]);
-            }
-            o[d] = bf16_of_double(v);
+        decode_row(layout, pool + phys * PB + row * CB, pool + phys * PB + P * CB + row * SB,
+                   out_bf16 + t * out_row_stride);
+    }
+    return rc;
+}
+
+/* Dequant of selected tokens (the consumer side of [P1] section 4: only the
+ * slots a sparse attention picks): out row i = the token in slot slots[i].
+ * Slot -1 is padding and gives a zero row; any other slot outside the pool
+ * leaves row i untouched and returns the out-of-range status. */
+int or_dequant_slots(int layout, int page_bits, const uint8_t *pool, int64_t pool_slots,
+                     const int64_t *slots, int64_t n, uint16_t *out_bf16, int64_t out_row_stride)
+{
+    if (!valid_layout(layout) || page_bits < 1 || page_bits > 16 || n < 0) return OR_EINVAL;
+    int rc = OR_OK;
+    for (int64_t i = 0; i < n; ++i) {
+        uint16_t *o = out_bf16 + i * out_row_stride;
+        int64_t s = slots[i];
+        if (s == -1) {
+            for (int d = 0; d < OR_D; ++d) o[d] = 0;
+            continue;
         }
+        if (s < 0 || s >= pool_slots) { rc = OR_ERANGE; continue; }
+        uint8_t *crow, *srow;
+        slot_addresses(layout, page_bits, (uint8_t *)pool, s, &crow, &srow);
+        decode_row(layout, crow, srow, o);
     }
     return rc;
 }

@@ -82,6 +82,9 @@ int or_dequant(int layout, int page_bits, const uint8_t *pool, int64_t pool_page
                const int32_t *page_table, int64_t n_tokens,
                uint16_t *out_bf16, int64_t out_row_stride);
 
+int or_dequant_slots(int layout, int page_bits, const uint8_t *pool, int64_t pool_slots,
+                     const int64_t *slots, int64_t n, uint16_t *out_bf16, int64_t out_row_stride);
+
 int or_translate(const int64_t *loc, int64_t n, const int32_t *full_to_swa,
                  int64_t full_slots, int32_t *out, int64_t capacity);
 

@@ -19,7 +19,7 @@ __all__ = [
     "bf16_round", "bf16_to_f32", "code_bytes", "scale_bytes", "bytes_per_token",
     "page_bytes", "encode_v41", "encode_fp4", "rmsnorm", "rope", "pool",
     "token_prequant", "group_prequant", "token_bytes", "group_bytes", "store",
-    "compress", "dequant", "translate",
+    "compress", "dequant", "dequant_slots", "translate",
 ]
 
 V41, FP4 = 1, 2
@@ -86,6 +86,8 @@ _SIGS = {
                               _p(C.c_int32), _p(C.c_int64), _p(C.c_uint8), C.c_int64]),
     "or_dequant": (C.c_int, [C.c_int, C.c_int, _p(C.c_uint8), C.c_int64, _p(C.c_int32),
                              C.c_int64, _p(C.c_uint16), C.c_int64]),
+    "or_dequant_slots": (C.c_int, [C.c_int, C.c_int, _p(C.c_uint8), C.c_int64, _p(C.c_int64),
+                                   C.c_int64, _p(C.c_uint16), C.c_int64]),
     "or_translate": (C.c_int, [_p(C.c_int64), C.c_int64, _p(C.c_int32), C.c_int64,
                                _p(C.c_int32), C.c_int64]),
 }
@@ -330,6 +332,17 @@ def dequant(layout, page_bits, pool_bytes, page_table, n_tokens):
     out = np.zeros((n_tokens, D), np.uint16)
     rc = lib().or_dequant(layout, page_bits, _ptr(pool_bytes, C.c_uint8), pool_pages,
                           _ptr(pt, C.c_int32), n_tokens, _ptr(out, C.c_uint16), D)
+    return rc, out
+
+
+def dequant_slots(layout, pool_bytes, slots, page_bits=6, out=None):
+    """Returns (status, bf16 bits uint16 [n, 512]) of the tokens in `slots`."""
+    slots = _arr(slots, np.int64)
+    pool_slots = pool_bytes.size // bytes_per_token(layout)
+    if out is None:
+        out = np.full((slots.size, D), 0xBEEF, np.uint16)
+    rc = lib().or_dequant_slots(layout, page_bits, _ptr(pool_bytes, C.c_uint8), pool_slots,
+                                _ptr(slots, C.c_int64), slots.size, _ptr(out, C.c_uint16), D)
     return rc, out
 
 

@@ -108,3 +108,19 @@ def test_translate_rejects_on_host(L):
     assert L.kvq_translate_loc(None, 1, 4, A, 100, A, 9, None, None) == 1
     assert L.kvq_translate_loc(A + 4, 1, 4, A, 100, A, 9, None, None) == 1  # int64 misaligned
     assert L.kvq_translate_loc(A, 0, 0, A, 100, A, 0, None, None) == 0
+
+
+def test_dequant_slots_rejects_on_host(L):
+    def d(layout=1, page_bits=6, pool=A, slots_n=64, idx=A, dt=0, n=4, out=A, stride=512):
+        return L.kvq_dequant_slots(layout, page_bits, pool, slots_n, idx, dt, n, out, stride, None, None)
+    assert d(layout=5) == 1
+    assert d(page_bits=3) == 2
+    assert d(pool=A + 8) == 1
+    assert d(slots_n=65) == 1
+    assert d(dt=3) == 1
+    assert d(idx=None) == 1
+    assert d(idx=A + 4, dt=1) == 1
+    assert d(out=A + 8) == 1
+    assert d(stride=256) == 1
+    assert d(n=-1) == 1
+    assert d(n=0, idx=None, out=None) == 0

@@ -467,3 +467,139 @@ def test_error_paths(K):
     torch.cuda.synchronize()
     assert outb.cpu().tolist() == [2, -1, -1, 0]
     assert err.item() == K.kvq.DEVERR_LOC
+
+
+# --------------------------------------------------------------------------- one step across layers
+
+def test_step_translates_once_for_all_layers(K):
+    """One decode step of a 3-layer model: the step's full-pool slots are
+    translated to SWA slots once and every layer's store uses them.  The pools
+    equal those written with the translation repeated inside every layer, and
+    each layer equals the oracle (RoPE store: bit-exact)."""
+    from compress_kv_write_gb300 import synth
+    L, n, full_slots, swa_slots = 3, 200, 1 << 14, 1 << 10
+    full_loc = synth.injective_slots(n, full_slots, DEV, 5)
+    table = synth.swa_table(full_slots, swa_slots, full_loc, DEV, 5)
+    xs = [synth.store_rows_bf16(n, DEV, 50 + l) for l in range(L)]
+    pos = synth.positions(n, DEV, 5, max_pos=4096)
+    cs = synth.rope_table(4096, DEV)
+    swa = torch.zeros(n, dtype=torch.int32, device=DEV)
+    hoisted = [torch.zeros(swa_slots * 528, dtype=torch.uint8, device=DEV) for _ in range(L)]
+    per_layer = [torch.zeros(swa_slots * 528, dtype=torch.uint8, device=DEV) for _ in range(L)]
+    err = _err(K)
+    K.kvq_translate_loc(full_loc, table, swa, err=err)
+    for l in range(L):
+        K.kvq_store(K.V41, 6, K.FLAG_ROPE, xs[l], swa, hoisted[l], swa_slots, cos_sin=cs, pos=pos, err=err)
+    for l in range(L):
+        swa_l = torch.full((n,), -7, dtype=torch.int32, device=DEV)
+        K.kvq_translate_loc(full_loc, table, swa_l, err=err)
+        K.kvq_store(K.V41, 6, K.FLAG_ROPE, xs[l], swa_l, per_layer[l], swa_slots, cos_sin=cs, pos=pos, err=err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    rc, tr = O.translate(full_loc.cpu().numpy(), table.cpu().numpy(), n)
+    assert rc == O.OK
+    for l in range(L):
+        assert torch.equal(hoisted[l], per_layer[l])
+        ref = np.zeros(swa_slots * 528, np.uint8)
+        assert O.store(O.V41, 6, O.ROPE, _bf16_np(xs[l]), tr, ref, cos_sin=cs.cpu().numpy(),
+                       pos=pos.cpu().numpy()) == O.OK
+        assert (np_u8(hoisted[l]) == ref).all()
+
+
+# --------------------------------------------------------------------------- selected-slot dequant
+
+@pytest.mark.parametrize("layout", [1, 2])
+@pytest.mark.parametrize("page_bits", [2, 6])
+def test_dequant_slots_small(K, layout, page_bits):
+    """Random, repeated, padding (-1) and out-of-range slots: bit-exact rows,
+    untouched rows for bad slots, the slot error bit set."""
+    from compress_kv_write_gb300 import synth
+    slots_n = 512
+    x = synth.student_t_rows_bf16(300, "cpu", 9)
+    loc = synth.injective_slots(300, slots_n, "cpu", 9)
+    pool_o = np.zeros(slots_n * O.bytes_per_token(layout), np.uint8)
+    assert O.store(layout, page_bits, 0, _bf16_np(x), loc.numpy(), pool_o) == O.OK
+    pool = torch.from_numpy(pool_o).to(DEV)
+    rng = np.random.default_rng(layout * 10 + page_bits)
+    for idx_dtype in (torch.int32, torch.int64):
+        sel = rng.integers(0, slots_n, 203)
+        sel[[3, 50, 51]] = -1
+        sel[[7, 100]] = [slots_n, -5]
+        slots = torch.as_tensor(sel, dtype=idx_dtype, device=DEV)
+        out = torch.full((sel.size, 512), 3.0, dtype=torch.bfloat16, device=DEV)
+        err = _err(K)
+        K.kvq_dequant_slots(layout, page_bits, pool, slots_n, slots, out, err=err)
+        torch.cuda.synchronize()
+        assert err.item() == K.kvq.DEVERR_SLOT
+        ref_out = np.full((sel.size, 512), O.bf16_bits(np.float32(3.0)), np.uint16)
+        rc, ref = O.dequant_slots(layout, pool_o, sel, page_bits, out=ref_out)
+        assert rc == O.ERANGE
+        assert (_bf16_np(out) == ref).all()
+
+
+def test_dequant_slots_fp4_pool_2m(K):
+    """262144 selected slots of a full 2^21-slot FP4 pool (every slot written)."""
+    from compress_kv_write_gb300 import synth
+    pool_slots, n = 1 << 21, 1 << 18
+    pool = torch.zeros(pool_slots * 288, dtype=torch.uint8, device=DEV)
+    chunk = 1 << 18
+    x = synth.student_t_rows_bf16(chunk, DEV, 3)
+    for c in range(pool_slots // chunk):
+        K.kvq_store(K.V41_FP4, 6, 0, x, torch.arange(c * chunk, (c + 1) * chunk, device=DEV), pool, pool_slots)
+    sel = synth.injective_slots(n, pool_slots, DEV, 4)
+    out = torch.empty((n, 512), dtype=torch.bfloat16, device=DEV)
+    err = _err(K)
+    K.kvq_dequant_slots(K.V41_FP4, 6, pool, pool_slots, sel, out, err=err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    rng = np.random.default_rng(0)
+    pick = rng.choice(n, 4096, replace=False)
+    sel_np = sel.cpu().numpy()
+    pool_np = np_u8(pool)
+    rc, ref = O.dequant_slots(O.FP4, pool_np, sel_np[pick], 6)
+    assert rc == O.OK
+    assert (_bf16_np(out[torch.as_tensor(pick, device=DEV)]) == ref).all()
+
+
+# --------------------------------------------------------------------------- more page sizes
+
+@pytest.mark.parametrize("page_bits", [4, 8])
+@pytest.mark.parametrize("layout", [1, 2])
+def test_page_sizes_16_and_256(K, page_bits, layout):
+    """Pages of 16 and 256 tokens: store + RoPE, ratio-1 compressor (identity,
+    bit-exact), paged dequant through a permuted page table and the
+    selected-slot dequant, all against the oracle."""
+    from compress_kv_write_gb300 import synth
+    P = 1 << page_bits
+    pages = 8
+    slots = pages * P
+    n = min(300, slots // 2)
+    x = synth.store_rows_bf16(n, "cpu", page_bits)
+    loc = synth.injective_slots(n, slots, "cpu", page_bits)
+    cs = synth.rope_table(1024, "cpu")
+    pos = synth.positions(n, "cpu", page_bits, max_pos=1024)
+    pool_o = np.zeros(slots * O.bytes_per_token(layout), np.uint8)
+    assert O.store(layout, page_bits, O.ROPE, _bf16_np(x), loc.numpy(), pool_o, cos_sin=cs.numpy(),
+                   pos=pos.numpy()) == O.OK
+    g = 20
+    v, s = synth.compressor_rows(g, "cpu", page_bits)
+    cloc = torch.as_tensor(np.setdiff1d(np.arange(slots), loc.numpy())[:g], dtype=torch.int32)
+    assert O.compress(layout, page_bits, 1, 0, v.numpy(), s.numpy(), cloc.numpy(), pool_o) == O.OK
+    pool = torch.zeros(slots * O.bytes_per_token(layout), dtype=torch.uint8, device=DEV)
+    err = _err(K)
+    K.kvq_store(layout, page_bits, K.FLAG_ROPE, x.to(DEV), loc.to(DEV), pool, slots, cos_sin=cs.to(DEV),
+                pos=pos.to(DEV), err=err)
+    K.kvq_compress(layout, page_bits, 1, 0, v.to(DEV), s.to(DEV), cloc.to(DEV), pool, slots, err=err)
+    pt = synth.page_table_perm(pages, "cpu", page_bits)
+    ws = torch.empty((slots, 512), dtype=torch.bfloat16, device=DEV)
+    K.kvq_dequant(layout, page_bits, pool, pages, pt.to(DEV), ws, err=err)
+    sel = torch.as_tensor(np.random.default_rng(page_bits).integers(-1, slots, 97), dtype=torch.int64)
+    gs = torch.empty((97, 512), dtype=torch.bfloat16, device=DEV)
+    K.kvq_dequant_slots(layout, page_bits, pool, slots, sel.to(DEV), gs, err=err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    assert (np_u8(pool) == pool_o).all()
+    rc, ref = O.dequant(layout, page_bits, pool_o, pt.numpy(), slots)
+    assert rc == O.OK and (_bf16_np(ws) == ref).all()
+    rc, ref = O.dequant_slots(layout, pool_o, sel.numpy(), page_bits)
+    assert rc == O.OK and (_bf16_np(gs) == ref).all()

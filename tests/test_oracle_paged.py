@@ -151,3 +151,30 @@ def test_translate_capacity_and_range():
     rc, out = O.translate(np.array([1, 16, -1, 2]), table, 6)
     assert rc == O.ERANGE
     assert list(out) == [3, -1, -1, 6, 0, 0]
+
+
+@pytest.mark.parametrize("layout", [O.V41, O.FP4])
+def test_dequant_slots_equals_paged_rows(layout):
+    """Selected-slot dequant returns exactly the rows the paged dequant gives
+    for those slots (identity page table); -1 is a zero row."""
+    page_bits, pages = 2, 8
+    P = 1 << page_bits
+    rng = np.random.default_rng(65)
+    x = (rng.standard_t(3, (20, 512)) * 0.5).astype(np.float32)
+    loc = rng.permutation(pages * P)[:20]
+    pool = np.zeros(pages * P * O.bytes_per_token(layout), np.uint8)
+    assert O.store(layout, page_bits, 0, x, loc, pool) == O.OK
+    rc, full = O.dequant(layout, page_bits, pool, np.arange(pages, dtype=np.int32), pages * P)
+    assert rc == O.OK
+    for slots in (np.arange(pages * P), rng.permutation(pages * P)[:11], np.array([5, -1, 5, 0])):
+        rc, got = O.dequant_slots(layout, pool, slots, page_bits)
+        assert rc == O.OK
+        for i, s in enumerate(slots):
+            assert (got[i] == (0 if s == -1 else full[s])).all()
+
+
+def test_dequant_slots_range_rule():
+    pool = np.zeros(8 * 528, np.uint8)
+    rc, got = O.dequant_slots(O.V41, pool, np.array([1, 8, -2]), 2)
+    assert rc == O.ERANGE
+    assert (got[0] == 0).all() and (got[1:] == 0xBEEF).all()
