@@ -49,7 +49,7 @@ def b_compress(r, payload=528):
 DEFAULT_STEPS = {
     "store_norm_rope": 200000, "store_rope": 200000, "store": 200000, "small": 200000,
     "fp4_store": 20000, "fp4_dequant": 3000, "c4a": 20000, "c128a": 1000, "c128a_fp4": 1000,
-    "layers": 2000, "dequant_select": 3000,
+    "layers": 2000, "dequant_select": 3000, "c4a_decode": 20000,
 }
 
 # the workloads: one per configuration of the write path
@@ -60,6 +60,9 @@ SPECS = {
     "store_norm_rope": dict(kind="store", flags=3, bs=16384, pool_slots=1 << 20, layout=1),
     "fp4_store": dict(kind="store", flags=0, bs=262144, pool_slots=1 << 21, layout=2, student_t=True),
     "fp4_dequant": dict(kind="dequant", pool_slots=1 << 21, layout=2),
+    # decode-time C4A: one new row per request per step, the open group's softmax carried as state
+    "c4a_decode": dict(kind="decode", ratio=4, layout=1, requests=16384, pool_slots=1 << 17,
+                       score_std=math.sqrt(2.0)),
     # the consumer side: the rows a sparse attention selects, gathered by slot
     "dequant_select": dict(kind="select", pool_slots=1 << 21, layout=2, n=1 << 18),
     "c4a": dict(kind="compress", ratio=4, layout=1, score_std=math.sqrt(2.0), groups=16384,
@@ -94,6 +97,11 @@ def describe(name):
         return {"workload": name, "layout": lay, "tokens": sp["pool_slots"], "page_size": 64,
                 "page_table": "random permutation of the pool's pages",
                 "rows": "0.5*Student-t(3) stored by the FP4 store"}, "tokens"
+    if sp["kind"] == "decode":
+        return {"workload": name, "layout": lay, "ratio": sp["ratio"], "requests": sp["requests"],
+                "state": "3 x 512 fp32 per request (running max, sum, weighted sum)",
+                "phases": "request i starts at count i % ratio: a quarter complete a group each step",
+                "pool_slots": sp["pool_slots"], "page_size": 64, "rope": "last 64 dims"}, "input tokens"
     if sp["kind"] == "select":
         return {"workload": name, "layout": lay, "pool_slots": sp["pool_slots"], "selected": sp["n"],
                 "slots": "random distinct int64 slots of the whole pool", "page_size": 64,
@@ -351,6 +359,61 @@ class CompressWorkload(Workload):
         self.herr.copy_(self.err, non_blocking=True)
 
 
+class DecodeWorkload(Workload):
+    """Decode-time ratio-r compressor over many requests, one row each per step."""
+
+    def __init__(self, name, dev):
+        super().__init__(name, dev)
+        import torch
+        from compress_kv_write_gb300 import synth
+        sp = self.spec
+        self.r, self.layout, self.n, self.pool_slots = sp["ratio"], sp["layout"], sp["requests"], sp["pool_slots"]
+        self.R = 4
+        self.v, self.s = [], []
+        for k in range(self.R):
+            v, s = synth.compressor_rows(self.n, dev, k, score_std=sp["score_std"])
+            self.v.append(v)
+            self.s.append(s)
+        self.state = torch.zeros((self.n, 3, 512), dtype=torch.float32, device=dev)
+        self.count = (torch.arange(self.n, dtype=torch.int32, device=dev) % self.r).contiguous()
+        self.loc = synth.injective_slots(self.n, self.pool_slots, dev, 0, dtype=torch.int32)
+        self.gpos = synth.positions(self.n, dev, 0)
+        self.cs = synth.rope_table(65536, dev)
+        self.pool = torch.zeros(self.pool_slots * self.K.bytes_per_token(self.layout), dtype=torch.uint8,
+                                device=dev)
+        payload = 528 if self.layout == 1 else 272
+        r = self.r
+        self.units = self.n
+        self.bytes_total = self.bytes_dominant = int(
+            self.n * (4096 + 8) + self.n * (r - 1) / r * 6144 * 2 + self.n / r * (4 + 4 + 256 + payload))
+        self.dominant = "compress_decode_kernel"
+        self.config["l2"] = (f"rotating {self.R} row sets of {self.n * 4096 / 2**20:.0f} MB; state "
+                             f"{self.n * 6144 / 2**20:.0f} MB read and written every step")
+
+    def _call(self, v, s):
+        self.K.kvq_compress_decode(self.layout, 6, self.r, self.K.FLAG_ROPE, v, s, self.state, self.count,
+                                   self.loc, self.pool, self.pool_slots, cos_sin=self.cs,
+                                   group_pos=self.gpos, err=self.err)
+
+    def step(self, i):
+        self._call(self.v[i % self.R], self.s[i % self.R])
+
+    def e2e_setup(self):
+        import torch
+        self.hv = self.v[0].cpu().pin_memory()
+        self.hs = self.s[0].cpu().pin_memory()
+        self.dv = torch.empty_like(self.v[0])
+        self.ds = torch.empty_like(self.s[0])
+        self.herr = torch.zeros(1, dtype=torch.int32).pin_memory()
+        return 2 * self.hv.numel() * 4, 4
+
+    def e2e_step(self):
+        self.dv.copy_(self.hv, non_blocking=True)
+        self.ds.copy_(self.hs, non_blocking=True)
+        self._call(self.dv, self.ds)
+        self.herr.copy_(self.err, non_blocking=True)
+
+
 class SelectWorkload(Workload):
     """Dequant of the rows a sparse attention selects from a full FP4 pool."""
 
@@ -481,6 +544,8 @@ def make_workload(name, dev, tokens=None):
             sp["bs"] = max(1, int(tokens) // sp["layers"])
         elif sp["kind"] == "select":
             sp["n"] = int(tokens)
+        elif sp["kind"] == "decode":
+            sp["requests"] = int(tokens)
         elif sp["ratio"] == 4:
             sp["groups"] = max(1, int(tokens) // 4)
         else:
@@ -488,7 +553,7 @@ def make_workload(name, dev, tokens=None):
         SPECS[name] = sp
     kind = SPECS[name]["kind"]
     cls = {"store": StoreWorkload, "dequant": DequantWorkload, "compress": CompressWorkload,
-           "layers": LayersWorkload, "select": SelectWorkload}[kind]
+           "layers": LayersWorkload, "select": SelectWorkload, "decode": DecodeWorkload}[kind]
     return cls(name, dev)
 
 
@@ -561,7 +626,7 @@ def measured_hbm_peak():
 
 
 KERNEL_SOURCES = {"store": "kvq_store.cu", "dequant": "kvq_dequant.cu", "compress": "kvq_compress.cu",
-                  "layers": "kvq_store.cu", "select": "kvq_dequant.cu"}
+                  "layers": "kvq_store.cu", "select": "kvq_dequant.cu", "decode": "kvq_compress.cu"}
 
 
 def traffic_from_profiles(workload):
@@ -824,7 +889,7 @@ def oracle_sample(name, n_rows):
         pool = np.zeros(n_pages * 64 * 288, np.uint8)
         assert O.store(O.FP4, 6, 0, x_np, np.arange(n_pages * 64), pool) == O.OK
         return dict(pages=pool)
-    r = spec["ratio"]
+    r = spec["ratio"]  # compress and decode: the oracle pools whole groups of r rows
     g = max(1, n_rows // r)
     v, s = synth.compressor_rows(g * r, "cpu", 0, score_std=spec["score_std"])
     return dict(v=v.numpy(), s=s.numpy(), gpos=(np.arange(g, dtype=np.int32) * r),
@@ -869,14 +934,14 @@ def oracle_run(name, smp, n_units):
 
 def _sample_rows(name):
     spec = SPECS[name]
-    if spec["kind"] == "compress":
+    if spec["kind"] in ("compress", "decode"):
         return spec["ratio"] * (16 if spec["ratio"] >= 128 else 1024)
     return min(4096, spec.get("bs", 4096))
 
 
 def _chunk_units(name):
     spec = SPECS[name]
-    if spec["kind"] == "compress":
+    if spec["kind"] in ("compress", "decode"):
         return spec["ratio"] * (1 if spec["ratio"] >= 128 else 64)
     return min(256, spec.get("bs", 256))
 
@@ -911,7 +976,8 @@ def run_reference(args):
     u0 = oracle_run(name, smp, chunk)
     per_unit = (time.perf_counter() - t0) / u0
     per_step = int(args.ref_seconds / max(1, K + W) / per_unit)
-    per_step = max(chunk if SPECS[name]["kind"] == "compress" else 1, min(per_step, _sample_rows(name)))
+    per_step = max(chunk if SPECS[name]["kind"] in ("compress", "decode") else 1,
+                   min(per_step, _sample_rows(name)))
     for _ in range(W):
         oracle_run(name, smp, per_step)
     done = 0

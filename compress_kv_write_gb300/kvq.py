@@ -18,7 +18,7 @@ V41, V41_FP4 = 1, 2
 F32, BF16 = 0, 1
 I32, I64 = 0, 1
 FLAG_ROPE, FLAG_NORM = 1, 2
-DEVERR_SLOT, DEVERR_POS, DEVERR_PAGE, DEVERR_LOC = 1, 2, 4, 8
+DEVERR_SLOT, DEVERR_POS, DEVERR_PAGE, DEVERR_LOC, DEVERR_TIMEOUT, DEVERR_STATE = 1, 2, 4, 8, 16, 32
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CAPACITY, ERR_LAUNCH = 0, 1, 2, 3, 4
 HEAD_DIM = 512
 
@@ -45,6 +45,10 @@ _SIGS = {
     "kvq_compress": (C.c_int, [C.c_int, C.c_int, C.c_int, C.c_uint, C.c_void_p, C.c_void_p,
                                C.c_int64, C.c_void_p, C.c_int64, C.c_void_p, C.c_void_p,
                                C.c_void_p, C.c_int64, C.c_void_p, C.c_void_p]),
+    "kvq_compress_decode": (C.c_int, [C.c_int, C.c_int, C.c_int, C.c_uint, C.c_void_p, C.c_void_p,
+                                      C.c_int64, C.c_void_p, C.c_void_p, C.c_void_p, C.c_int64,
+                                      C.c_void_p, C.c_int64, C.c_void_p, C.c_void_p, C.c_void_p,
+                                      C.c_int64, C.c_void_p, C.c_void_p]),
     "kvq_dequant_slots": (C.c_int, [C.c_int, C.c_int, C.c_void_p, C.c_int64, C.c_void_p, C.c_int,
                                     C.c_int64, C.c_void_p, C.c_int64, C.c_void_p, C.c_void_p]),
     "kvq_dequant": (C.c_int, [C.c_int, C.c_int, C.c_void_p, C.c_int64, C.c_void_p, C.c_int64,
@@ -248,3 +252,53 @@ def kvq_dequant_slots(layout, page_bits, pool, pool_slots, slots, out, err=None,
                                  _idx_dtype(slots, "slots"), slots.numel(), _ptr(out), out.stride(0),
                                  _ptr(err), _stream(stream))
     _check(st, "kvq_dequant_slots")
+
+
+def kvq_compress_decode(layout, page_bits, ratio, flags, values, scores, state, count, loc, pool,
+                        pool_slots, *, req=None, cos_sin=None, group_pos=None, err=None, stream=None):
+    """One decode step of the ratio-r compressor: request i appends row
+    (values[i], scores[i]) to the open group held in state[req[i]] /
+    count[req[i]]; a group's ratio-th row pools, quantises and stores it into
+    slot loc[i]."""
+    _cuda(values, "values", (torch.float32,))
+    _cuda(scores, "scores", (torch.float32,))
+    _cuda(state, "state", (torch.float32,))
+    _cuda(count, "count", (torch.int32,))
+    _cuda(loc, "loc", (torch.int32,))
+    _cuda(pool, "pool", (torch.uint8,))
+    if values.shape != scores.shape or values.dim() != 2 or values.shape[1] != HEAD_DIM:
+        raise ValueError("values and scores must both be [n, 512]")
+    if not values.is_contiguous() or not scores.is_contiguous():
+        raise ValueError("values and scores must be contiguous")
+    n = values.shape[0]
+    if state.dim() != 3 or state.shape[1:] != (3, HEAD_DIM) or not state.is_contiguous():
+        raise ValueError("state must be contiguous [n_state, 3, 512]")
+    _contig1d(count, "count")
+    if count.numel() != state.shape[0]:
+        raise ValueError("count must hold one entry per state row")
+    _contig1d(loc, "loc")
+    if loc.numel() != n:
+        raise ValueError("loc must hold one slot per request")
+    if req is not None:
+        _cuda(req, "req", (torch.int32,))
+        _contig1d(req, "req")
+        if req.numel() != n:
+            raise ValueError("req must hold one state index per request")
+    if pool.numel() < pool_slots * bytes_per_token(layout):
+        raise ValueError("pool is smaller than pool_slots tokens")
+    rows = 0
+    if cos_sin is not None:
+        _cuda(cos_sin, "cos_sin", (torch.float32,))
+        if cos_sin.dim() != 2 or cos_sin.shape[1] != 64 or not cos_sin.is_contiguous():
+            raise ValueError("cos_sin must be contiguous [rows, 64]")
+        rows = cos_sin.shape[0]
+    if group_pos is not None:
+        _cuda(group_pos, "group_pos", (torch.int32,))
+        _contig1d(group_pos, "group_pos")
+        if group_pos.numel() != n:
+            raise ValueError("group_pos must hold one position per request")
+    st = lib().kvq_compress_decode(layout, page_bits, ratio, flags, _ptr(values), _ptr(scores), n,
+                                   _ptr(state), _ptr(count), _ptr(req), state.shape[0], _ptr(cos_sin),
+                                   rows, _ptr(group_pos), _ptr(loc), _ptr(pool), int(pool_slots),
+                                   _ptr(err), _stream(stream))
+    _check(st, "kvq_compress_decode")

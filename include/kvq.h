@@ -70,8 +70,10 @@ enum {
     KVQ_DEVERR_POS = 2,   /* a RoPE position outside [0, cos_sin_rows) (skipped) */
     KVQ_DEVERR_PAGE = 4,  /* a page-table entry outside [0, pool_pages) (skipped)*/
     KVQ_DEVERR_LOC = 8,   /* a full slot outside the translation table (-> -1)   */
-    KVQ_DEVERR_TIMEOUT = 16 /* an internal pipeline wait ran past its 2 s limit;  */
-                            /* the kernel stopped early (output incomplete)       */
+    KVQ_DEVERR_TIMEOUT = 16, /* an internal pipeline wait ran past its 2 s limit; */
+                             /* the kernel stopped early (output incomplete)      */
+    KVQ_DEVERR_STATE = 32    /* a request index outside [0, n_state) or a count   */
+                             /* outside [0, ratio): that request is skipped       */
 };
 
 /* Bytes one token occupies: 528 (V41) or 288 (V41_FP4); 0 for a bad layout.
@@ -138,6 +140,31 @@ kvq_status kvq_compress(kvq_layout layout, int page_bits, int ratio, unsigned fl
                         const float *cos_sin, int64_t cos_sin_rows, const int32_t *group_pos,
                         const int32_t *loc, uint8_t *pool, int64_t pool_slots,
                         int32_t *err, struct CUstream_st *stream);
+
+/* Decode-time ratio-r compressor ([P1] section 2, flash_c1/c2_decode_kernel;
+ * [P3] section 2, the online max / sum softmax): each call brings ONE new row
+ * per request, and the softmax pool of the request's unfinished group is
+ * carried between calls as online state.
+ *   values, scores  [n, 512] fp32: request i's new row.
+ *   state           [n_state, 3, 512] fp32, caller-owned, per request slot:
+ *                   running max m, sum of exp(s - m) and sum of
+ *                   exp(s - m) * v of the rows seen so far, per dim.
+ *   count           [n_state] int32: rows of the open group (0 .. ratio-1);
+ *                   start at 0 with any state contents.
+ *   req             [n] int32: state slot of request i (NULL: slot i).
+ * When request i's row is the group's ratio-th, the pooled row acc / sum is
+ * rotated by row group_pos[i] of cos_sin (KVQ_FLAG_ROPE), rounded to bf16,
+ * quantised and stored into slot loc[i] exactly as kvq_compress does, and
+ * count returns to 0; otherwise only state and count change and loc[i],
+ * group_pos[i] are not read.  A bad request index or count sets
+ * KVQ_DEVERR_STATE and skips that request.  Requests in one call must use
+ * distinct state slots.  KVQ_FLAG_NORM is not accepted. */
+kvq_status kvq_compress_decode(kvq_layout layout, int page_bits, int ratio, unsigned flags,
+                               const float *values, const float *scores, int64_t n,
+                               float *state, int32_t *count, const int32_t *req, int64_t n_state,
+                               const float *cos_sin, int64_t cos_sin_rows, const int32_t *group_pos,
+                               const int32_t *loc, uint8_t *pool, int64_t pool_slots,
+                               int32_t *err, struct CUstream_st *stream);
 
 /* Paged dequant to a bf16 workspace ([P1] section 4, dequant_k_cache.py).
  *   page_table  [n_tokens / 2^page_bits] int32: physical page of each

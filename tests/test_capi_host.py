@@ -124,3 +124,20 @@ def test_dequant_slots_rejects_on_host(L):
     assert d(stride=256) == 1
     assert d(n=-1) == 1
     assert d(n=0, idx=None, out=None) == 0
+
+
+def test_compress_decode_rejects_on_host(L):
+    def c(ratio=4, flags=0, v=A, s=A, n=8, state=A, count=A, req=None, n_state=8, loc=A, layout=1):
+        return L.kvq_compress_decode(layout, 6, ratio, flags, v, s, n, state, count, req, n_state,
+                                     None, 0, None, loc, A, 64, None, None)
+    assert c(ratio=3) == 2
+    assert c(ratio=0) == 1
+    assert c(flags=2) == 2
+    assert c(flags=1) == 1                 # RoPE without a table
+    assert c(state=None) == 1
+    assert c(state=A + 4) == 1
+    assert c(count=None) == 1
+    assert c(n=9, req=None, n_state=8) == 1  # more requests than state rows, no index
+    assert c(loc=None) == 1
+    assert c(n_state=0) == 1
+    assert c(n=0) == 0

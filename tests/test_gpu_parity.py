@@ -603,3 +603,83 @@ def test_page_sizes_16_and_256(K, page_bits, layout):
     assert rc == O.OK and (_bf16_np(ws) == ref).all()
     rc, ref = O.dequant_slots(layout, pool_o, sel.numpy(), page_bits)
     assert rc == O.OK and (_bf16_np(gs) == ref).all()
+
+
+# --------------------------------------------------------------------------- decode-time compressor
+
+@pytest.mark.parametrize("layout", [1, 2])
+@pytest.mark.parametrize("r", [1, 2, 4, 128])
+def test_compress_decode_streams(K, layout, r):
+    """Rows arrive one per call to a random subset of request slots, in random
+    order (state indexed through req); every group a slot completes is
+    compared with the oracle's pooling of that group's r rows.  r = 1 is the
+    identity (bit-exact); the others follow the pooling tolerance."""
+    rng = np.random.default_rng(100 * layout + r)
+    n_state = 24 if r < 128 else 6
+    calls = 3 * r + 2 if r < 128 else 2 * r + 3
+    pool_slots = max(1024, -(-calls * n_state // 64) * 64)  # a fresh destination per row
+    from compress_kv_write_gb300 import synth
+    cs = synth.rope_table(2048, DEV)
+    cs_np = cs.cpu().numpy()
+    state = torch.zeros((n_state, 3, 512), dtype=torch.float32, device=DEV)
+    count = torch.zeros(n_state, dtype=torch.int32, device=DEV)
+    pool = torch.zeros(pool_slots * O.bytes_per_token(layout), dtype=torch.uint8, device=DEV)
+    err = _err(K)
+    seen = [[] for _ in range(n_state)]  # rows each slot has received: (v, s)
+    groups = []                           # (slot, first row index, dest slot, pos)
+    free_slots = list(rng.permutation(pool_slots))
+    for call in range(calls):
+        active = np.flatnonzero(rng.random(n_state) < (0.8 if r < 128 else 1.0))
+        if active.size == 0:
+            continue
+        req = rng.permutation(active).astype(np.int32)
+        v = rng.standard_normal((req.size, 512)).astype(np.float32)
+        s = (rng.standard_normal((req.size, 512)) * 2).astype(np.float32)
+        loc = np.empty(req.size, np.int32)
+        gpos = np.empty(req.size, np.int32)
+        for j, rs in enumerate(req):
+            k = len(seen[rs])
+            seen[rs].append((v[j], s[j]))
+            loc[j] = free_slots.pop()
+            gpos[j] = (k // r) * r % 2048
+            if k % r == r - 1:
+                groups.append((rs, k - r + 1, loc[j], gpos[j]))
+        K.kvq_compress_decode(layout, 6, r, K.FLAG_ROPE, torch.from_numpy(v).to(DEV), torch.from_numpy(s).to(DEV),
+                              state, count, torch.from_numpy(loc).to(DEV), pool, pool_slots,
+                              req=torch.from_numpy(req).to(DEV), cos_sin=cs, group_pos=torch.from_numpy(gpos).to(DEV),
+                              err=err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    assert groups, "some groups completed"
+    assert (count.cpu().numpy() == np.array([len(x) % r for x in seen])).all()
+    got = np_u8(pool)
+    g = gather_rows(got, layout, 6, [x[2] for x in groups])
+    oc, osc, ys = [], [], []
+    for rs, k0, dst, pos in groups:
+        vv = np.stack([seen[rs][k][0] for k in range(k0, k0 + r)])
+        ss = np.stack([seen[rs][k][1] for k in range(k0, k0 + r)])
+        c_, s_ = O.group_bytes(layout, r, O.ROPE, vv, ss, cs_np[pos])
+        oc.append(c_)
+        osc.append(s_)
+        ys.append(O.group_prequant(r, O.ROPE, vv, ss, cs_np[pos]))
+    oc, osc = np.stack(oc), np.stack(osc)
+    if r == 1:
+        assert (g[0] == oc).all() and (g[1] == osc).all()
+    else:
+        check_tolerance(layout, g[0], g[1], oc, osc, np.stack(ys), budget=2e-3)
+    written = int(g[0].astype(np.int64).sum() + g[1].astype(np.int64).sum())
+    assert int(got.astype(np.int64).sum()) == written  # open groups wrote nothing
+
+
+def test_compress_decode_bad_state_index(K):
+    state = torch.zeros((2, 3, 512), dtype=torch.float32, device=DEV)
+    count = torch.tensor([0, 7], dtype=torch.int32, device=DEV)  # slot 1: count >= ratio
+    pool = torch.zeros(64 * 528, dtype=torch.uint8, device=DEV)
+    v = torch.ones((3, 512), device=DEV)
+    err = _err(K)
+    K.kvq_compress_decode(K.V41, 6, 4, 0, v, v, state, count, torch.tensor([1, 2, 3], dtype=torch.int32, device=DEV),
+                          pool, 64, req=torch.tensor([0, 1, 5], dtype=torch.int32, device=DEV), err=err)
+    torch.cuda.synchronize()
+    assert err.item() == K.kvq.DEVERR_STATE
+    assert count.cpu().tolist() == [1, 7]
+    assert int(pool.sum().item()) == 0
