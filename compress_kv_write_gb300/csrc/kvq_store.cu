@@ -74,8 +74,9 @@ template <bool kBf16, bool kRope>
 struct WarpStoreSmem {
     static constexpr int XB = kD * (kBf16 ? 2 : 4);    // input row bytes
     static constexpr int CSB = kRope ? kRopeD * 4 : 0;  // this token's cos/sin values
-    static constexpr int D = kBf16 ? 4 : 3;             // tokens in flight per warp
-    static constexpr int NS = D + 1;                    // ring slots per warp
+    static constexpr int D = 3;                         // tokens in flight per warp
+    static constexpr int NS = D + 1;                    // ring slots per warp (a power of two)
+    static_assert((NS & (NS - 1)) == 0, "ring index by mask");
     static constexpr int SLOT = XB + CSB;
     static constexpr int kWarpBytes = NS * SLOT;
     static constexpr int kBytes = kStoreWarps * kWarpBytes;
@@ -221,7 +222,7 @@ __global__ void __launch_bounds__(kStoreThreads) store_warp_kernel(const StoreAr
                 }
             }
             src_next += a.row_stride_bytes;
-            ring_in = ring_in == NS - 1 ? 0 : ring_in + 1;
+            ring_in = (ring_in + 1) & (NS - 1);
         }
         cp_async_commit();
     };
@@ -259,7 +260,7 @@ __global__ void __launch_bounds__(kStoreThreads) store_warp_kernel(const StoreAr
         }
         cp_async_wait<D - 1>();  // this lane's copies of token k have landed
         const uint8_t *slot_sm = wsm + ring_out * SM::SLOT;
-        ring_out = ring_out == NS - 1 ? 0 : ring_out + 1;
+        ring_out = (ring_out + 1) & (NS - 1);
         uint4 raw[K];
 #pragma unroll
         for (int kk = 0; kk < K; ++kk) raw[kk] = lds_u4(slot_sm + (kk * 32 + lane) * 16);
@@ -349,8 +350,9 @@ struct PairStoreSmem {
     static constexpr int CPR = kD / E;                  // chunks per row
     static constexpr int XB = kD * (kBf16 ? 2 : 4);     // row bytes
     static constexpr int CSB = kRope ? kRopeD * 4 : 0;  // cos/sin row bytes
-    static constexpr int D = kBf16 ? 2 : 1;             // token pairs in flight per warp
-    static constexpr int NS = D + 1;                    // ring slots per warp
+    static constexpr int D = kBf16 ? 3 : 1;             // token pairs in flight per warp
+    static constexpr int NS = D + 1;                    // ring slots per warp (a power of two)
+    static_assert((NS & (NS - 1)) == 0, "ring index by mask");
     static constexpr int SLOT = 2 * XB + 2 * CSB;
     static constexpr int kWarpBytes = NS * SLOT;
     static constexpr int kW = kStoreWarps * kWarpBytes;  // norm weights, swizzled
@@ -434,7 +436,7 @@ __global__ void __launch_bounds__(kStoreThreads, 4) store_pair_kernel(const Stor
                 if (t < cnt && pt >= 0)
                     cp_async16(slot + 2 * SM::XB + h * SM::CSB + bi * 16, a.cs + int64_t(pt) * kRopeD + bi * 4);
             }
-            ring_in = ring_in == NS - 1 ? 0 : ring_in + 1;
+            ring_in = (ring_in + 1) & (NS - 1);
         }
         cp_async_commit();
     };
@@ -457,7 +459,7 @@ __global__ void __launch_bounds__(kStoreThreads, 4) store_pair_kernel(const Stor
         cp_async_wait<D - 1>();  // this lane's copies of pair k have landed ...
         __syncwarp();            // ... and so have the other lanes'
         const uint8_t *slot_sm = wsm + ring_out * SM::SLOT;
-        ring_out = ring_out == NS - 1 ? 0 : ring_out + 1;
+        ring_out = (ring_out + 1) & (NS - 1);
 
         float v[kBlock];
         {
