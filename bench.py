@@ -202,29 +202,53 @@ class StoreWorkload(Workload):
         r = i % self.R
         self._store(self.x[r], self.loc[r], self.pos[r])
 
-    # end to end: the step's rows, slots and positions come from pinned host memory
+    # End to end: each step's rows, slots and positions arrive as ONE pinned host
+    # buffer [rows | slots | positions]; it is copied into one of two device
+    # buffers on a copy stream while the previous step's store runs, and the
+    # step's error word is read back.
     def e2e_setup(self):
         import torch
-        self.hx = self.x[0].cpu().pin_memory()
-        self.hloc = self.loc[0].cpu().pin_memory()
-        self.hpos = self.pos[0].cpu().pin_memory()
-        self.dx = torch.empty_like(self.x[0])
-        self.dloc = torch.empty_like(self.loc[0])
-        self.dpos = torch.empty_like(self.pos[0])
+        x0, l0, p0 = self.x[0], self.loc[0], self.pos[0]
+        self.e2e_parts = [(x0.numel() * x0.element_size(), x0.dtype, x0.shape),
+                          (l0.numel() * 8, torch.int64, l0.shape), (p0.numel() * 4, torch.int32, p0.shape)]
+        total = sum(b for b, _, _ in self.e2e_parts)
+        host = torch.empty(total, dtype=torch.uint8).pin_memory()
+        off = 0
+        for (b, dt, shp), t in zip(self.e2e_parts, (x0, l0, p0)):
+            host[off:off + b].copy_(t.cpu().contiguous().view(torch.uint8).reshape(-1))
+            off += b
+        self.hbuf = host
+        self.dbufs = [torch.empty(total, dtype=torch.uint8, device=self.dev) for _ in range(2)]
+        self.dviews = []
+        for d in self.dbufs:
+            views, off = [], 0
+            for b, dt, shp in self.e2e_parts:
+                views.append(d[off:off + b].view(dt).view(shp))
+                off += b
+            self.dviews.append(views)
+        self.copy_stream = torch.cuda.Stream(device=self.dev)
+        self.copied = [torch.cuda.Event() for _ in range(2)]
+        self.done = [torch.cuda.Event() for _ in range(2)]
+        for e in self.done:
+            e.record()
         self.herr = torch.zeros(1, dtype=torch.int32).pin_memory()
-        h2d = self.hx.numel() * self.hx.element_size() + self.hloc.numel() * 8
-        if self.flags & 1:
-            h2d += self.hpos.numel() * 4
-        return h2d, 4
+        self.e2e_i = 0
+        return total, 4
 
     def e2e_step(self):
-        self.dx.copy_(self.hx, non_blocking=True)
-        self.dloc.copy_(self.hloc, non_blocking=True)
-        if self.flags & 1:
-            self.dpos.copy_(self.hpos, non_blocking=True)
-        self._store(self.dx, self.dloc, self.dpos)
+        import torch
+        b = self.e2e_i & 1
+        self.e2e_i += 1
+        compute = torch.cuda.current_stream()
+        self.copy_stream.wait_event(self.done[b])       # the store that last read this buffer
+        with torch.cuda.stream(self.copy_stream):
+            self.dbufs[b].copy_(self.hbuf, non_blocking=True)
+            self.copied[b].record(self.copy_stream)
+        compute.wait_event(self.copied[b])
+        dx, dloc, dpos = self.dviews[b]
+        self._store(dx, dloc, dpos)
+        self.done[b].record(compute)
         self.herr.copy_(self.err, non_blocking=True)
-
 
 class DequantWorkload(Workload):
     """Full-pool paged dequant of a 2^21-slot FP4 pool into a bf16 workspace."""
