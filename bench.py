@@ -1023,13 +1023,87 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_sweep(args):
+    """Per-launch latency of the store family and the c1 / c2 decode compressors
+    at the small batches of the store-latency table ([P1], bs 1/8/64/512):
+    CUDA graphs of back-to-back launches on one set of inputs (hot L2, as a
+    latency microbenchmark), per-launch time = graph time / launches."""
+    import torch
+    rank, world, local = dist_env()
+    if rank != 0:
+        return
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import __graft_entry__
+    __graft_entry__.build()
+    import compress_kv_write_gb300 as K
+    from compress_kv_write_gb300 import synth
+    pool_slots = 1 << 20
+    pool = torch.zeros(pool_slots * 528, dtype=torch.uint8, device=dev)
+    cs = synth.rope_table(65536, dev)
+    w = synth.norm_weight(dev, 0)
+    stream = torch.cuda.Stream(device=dev)
+    reps = max(200, args.steps)
+
+    def timed(fn):
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                fn()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(reps):
+                fn()
+        with torch.cuda.stream(stream):
+            g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        with torch.cuda.stream(stream):
+            g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1e3 / reps
+
+    table = {}
+    for bs in (1, 8, 64, 512):
+        x = synth.store_rows_bf16(bs, dev, bs)
+        loc = synth.injective_slots(bs, pool_slots, dev, bs)
+        pos = synth.positions(bs, dev, bs)
+        for name, flags in (("store", 0), ("store + RoPE", 1), ("fused K norm + RoPE", 3)):
+            us = timed(lambda: K.kvq_store(1, 6, flags, x, loc, pool, pool_slots, norm_weight=w, eps=1e-6,
+                                           cos_sin=cs, pos=pos))
+            table.setdefault(name, {})[bs] = round(us, 3)
+        v, sc = synth.compressor_rows(bs, dev, bs)
+        loc32 = loc.to(torch.int32)
+        for name, r in (("c1", 1), ("c2", 2)):
+            state = torch.zeros((bs, 3, 512), dtype=torch.float32, device=dev)
+            count = torch.zeros(bs, dtype=torch.int32, device=dev)
+            us = timed(lambda: K.kvq_compress_decode(1, 6, r, K.FLAG_ROPE, v, sc, state, count, loc32, pool,
+                                                     pool_slots, cos_sin=cs, group_pos=pos))
+            table.setdefault(name, {})[bs] = round(us, 3)
+    us512 = table["fused K norm + RoPE"][512]
+    line = {
+        "metric": METRIC, "value": 512 / (us512 * 1e-6), "unit": "tokens/s", "n_gpus": 1, "steps": reps,
+        "warmup": 3, "ms_per_step": us512 / 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": "latency sweep (value: fused K norm + RoPE, V41, bs 512)",
+                   "layout": "V41", "x_dtype": "bf16", "pool_slots": pool_slots,
+                   "l2": "hot: one input set per batch size (latency microbenchmark)",
+                   "c1_c2": "kvq_compress_decode, ratio 1 / 2, one row per request, RoPE"},
+        "latency_us": table,
+        "gpu_launches": reps,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default="store_norm_rope",
-                    choices=sorted(DEFAULT_STEPS))
+                    choices=sorted(DEFAULT_STEPS) + ["sweep"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -1040,10 +1114,14 @@ def main(argv=None):
                     help="profiling only: shrink the workload to about this many tokens")
     args = ap.parse_args(argv)
     if args.steps is None:
-        args.steps = DEFAULT_STEPS[args.workload]
+        args.steps = DEFAULT_STEPS.get(args.workload, 1000)
     if args.warmup < 3:
         raise SystemExit("--warmup must be at least 3")
-    if args.impl == "reference":
+    if args.workload == "sweep":
+        if args.impl == "reference":
+            raise SystemExit("the latency sweep has no reference arm")
+        run_sweep(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

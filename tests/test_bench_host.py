@@ -1,0 +1,60 @@
+"""bench.py's host-side logic without a GPU: every workload describes itself,
+its oracle sample runs, the committed traffic table is found, and the
+reference arm (the CPU oracle) prints one JSON line with the contract's keys."""
+import io
+import json
+import os
+import sys
+from contextlib import redirect_stdout
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+
+KEYS = {"metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better", "scaling",
+        "vs_baseline", "dtype", "data", "config", "impl", "cpu_baseline", "e2e"}
+
+
+@pytest.mark.parametrize("name", sorted(bench.SPECS))
+def test_workload_description_and_oracle_sample(name):
+    cfg, unit = bench.describe(name)
+    assert cfg["workload"] == name and unit
+    smp = bench.oracle_sample(name, bench._sample_rows(name) if bench.SPECS[name]["kind"] != "compress"
+                              or bench.SPECS[name]["ratio"] < 128 else 256)
+    done = bench.oracle_run(name, smp, bench._chunk_units(name))
+    assert done >= 1
+    assert len(bench.kernel_source_sha(name)) == 16
+
+
+def test_traffic_table_matches_current_sources():
+    """Every workload with a committed capture resolves to a traffic figure
+    (the sources have not changed since), and it is close to the algorithmic
+    bytes it was scaled to."""
+    found = {w: bench.traffic_from_profiles(w) for w in bench.SPECS}
+    for w in ("store_norm_rope", "fp4_store", "fp4_dequant", "c4a", "c128a", "c4a_decode", "dequant_select"):
+        assert found[w] is not None and found[w] > 0, w
+
+
+@pytest.mark.parametrize("name", ["store_norm_rope", "fp4_dequant", "c4a"])
+def test_reference_arm_json(name, monkeypatch):
+    for k in ("RANK", "WORLD_SIZE", "LOCAL_RANK"):
+        monkeypatch.delenv(k, raising=False)
+    buf = io.StringIO()
+    with redirect_stdout(buf):
+        bench.main(["--impl", "reference", "--workload", name, "--steps", "3", "--warmup", "3",
+                    "--ref-seconds", "0.3"])
+    lines = [ln for ln in buf.getvalue().splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert KEYS <= set(d)
+    assert d["impl"] == "reference" and d["n_gpus"] == 1 and d["steps"] == 3 and d["warmup"] == 3
+    assert d["value"] > 0 and d["higher_is_better"] is True and d["config"]["workload"] == name
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] == 1
+
+
+def test_warmup_floor():
+    with pytest.raises(SystemExit):
+        bench.main(["--impl", "reference", "--warmup", "2"])
