@@ -1,9 +1,10 @@
-// kvq_compress.cu -- ratio-r per-element softmax compressor fused with RoPE,
-// bf16 rounding, block quantisation and the paged store.  Covers the c1/c2
+// kvq_compress.cu -- ratio-r per-element softmax compressor over whole
+// groups, fused with RoPE, bf16 rounding, block quantisation and the paged
+// store: the C4A / C128A compressors of "[vLLM] DeepSeek V4 Sparse FP8
+// Compressor kernel" (section 2: online max / sum softmax; section 3: RoPE,
+// bf16 cast, per-32-value absmax), and ratios 1 / 2 of the c1 / c2
 // compressors of "[sglang] DeepSeek V4.1 Paged KV Cache: V41 and FP4 formats"
-// (section 2) and the C4A / C128A compressors of "[vLLM] DeepSeek V4 Sparse
-// FP8 Compressor kernel" (section 2: online max / sum softmax; section 3:
-// RoPE, bf16 cast, per-32-value absmax).
+// (section 2).  The decode-time form is in kvq_decode.cu.
 //
 // Mapping: 128 threads per group; thread t owns dims 4t..4t+3 (one float4
 // column), so each row is one fully coalesced 2 KB sweep by the group's
@@ -18,7 +19,6 @@ namespace kvq {
 namespace {
 
 constexpr int kGroupThreads = 128;
-constexpr float kLog2e = 1.4426950408889634f;
 
 struct CompressArgs {
     const float *values;
@@ -32,12 +32,6 @@ struct CompressArgs {
     int64_t pool_slots;
     int32_t *err;
 };
-
-__device__ __forceinline__ float4 ld_f4(const float *p) {
-    uint4 r = ld_stream_u4(p);
-    return make_float4(__uint_as_float(r.x), __uint_as_float(r.y), __uint_as_float(r.z),
-                       __uint_as_float(r.w));
-}
 
 template <Layout L, int PageBits, int R, bool kRope, int GPC>
 __global__ void __launch_bounds__(kGroupThreads *GPC) compress_kernel(const CompressArgs a) {
@@ -183,173 +177,6 @@ kvq_status launch_compress(const CompressArgs &a, cudaStream_t stream) {
                       dim3(kGroupThreads * GPC), stream, a);
 }
 
-// ---------------------------------------------------------------------------
-// Decode-time compressor: one new row per request per call, the group's
-// softmax carried between calls as per-dim online state (running max m,
-// sum of exp(s - m) and sum of exp(s - m) * v), 3 x 512 fp32 per request.
-// One warp per request: lane l owns the float4 columns l, l+32, l+64, l+96,
-// so every warp access is one contiguous 512-byte span, a quant block is 8
-// adjacent lanes, and the request's count is read and rewritten by the same
-// warp (ordered by __syncwarp).
-
-constexpr int kDecWarps = 4;
-
-struct DecodeArgs {
-    const float *values;
-    const float *scores;
-    int64_t n;
-    float *state;
-    int32_t *count;
-    const int32_t *req;
-    int64_t n_state;
-    const float *cs;
-    int64_t cs_rows;
-    const int32_t *group_pos;
-    const int32_t *loc;
-    uint8_t *pool;
-    int64_t pool_slots;
-    int32_t *err;
-};
-
-template <Layout L, int PageBits, int R, bool kRope>
-__global__ void __launch_bounds__(kDecWarps * 32) compress_decode_kernel(const DecodeArgs a) {
-    using PK = PagedKV<L, PageBits>;
-    using T = LayoutTraits<L>;
-    constexpr int K = kD / 4 / 32;  // float4 columns per lane
-    const int lane = threadIdx.x & 31;
-    const int64_t i = int64_t(blockIdx.x) * kDecWarps + (threadIdx.x >> 5);
-    if (i >= a.n) return;  // whole warps; no block barrier follows
-    pdl_wait();
-
-    const int64_t ri = a.req ? int64_t(__ldg(a.req + i)) : i;
-    const int32_t c = (ri >= 0 && ri < a.n_state) ? a.count[ri] : -1;
-    __syncwarp();  // every lane has read the count before lane 0 rewrites it
-    if (c < 0 || c >= R) {
-        if (lane == 0) raise_err(a.err, KVQ_DEVERR_STATE);
-        return;
-    }
-    float4 m[K], l[K], acc[K];
-    float *st = a.state + ri * (3 * kD);
-#pragma unroll
-    for (int k = 0; k < K; ++k) {
-        const int col = 4 * (k * 32 + lane);
-        const float4 v = ld_f4(a.values + i * kD + col);
-        const float4 sc = ld_f4(a.scores + i * kD + col);
-        m[k] = sc;
-        l[k] = make_float4(1.f, 1.f, 1.f, 1.f);
-        acc[k] = v;
-        if (c > 0) {
-            const float4 m0 = *reinterpret_cast<const float4 *>(st + col);
-            const float4 l0 = *reinterpret_cast<const float4 *>(st + kD + col);
-            const float4 a0 = *reinterpret_cast<const float4 *>(st + 2 * kD + col);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float mo = (&m0.x)[e], so = (&sc.x)[e];
-                const float mn = fmaxf(mo, so);
-                const float al = ex2_approx((mo - mn) * kLog2e);
-                const float p = ex2_approx((so - mn) * kLog2e);
-                (&m[k].x)[e] = mn;
-                (&l[k].x)[e] = fmaf((&l0.x)[e], al, p);
-                (&acc[k].x)[e] = fmaf(p, (&v.x)[e], (&a0.x)[e] * al);
-            }
-        }
-    }
-    pdl_trigger();
-    if (c + 1 < R) {  // the group is still open: keep the state
-#pragma unroll
-        for (int k = 0; k < K; ++k) {
-            const int col = 4 * (k * 32 + lane);
-            *reinterpret_cast<float4 *>(st + col) = m[k];
-            *reinterpret_cast<float4 *>(st + kD + col) = l[k];
-            *reinterpret_cast<float4 *>(st + 2 * kD + col) = acc[k];
-        }
-        if (lane == 0) a.count[ri] = c + 1;
-        return;
-    }
-    // the group is complete: pool, rotate, round, quantise, store; restart
-    if (lane == 0) a.count[ri] = 0;
-    float y[K][4];
-#pragma unroll
-    for (int k = 0; k < K; ++k)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) y[k][e] = __fdiv_rn((&acc[k].x)[e], (&l[k].x)[e]);
-    bool pos_ok = true;
-    if constexpr (kRope) {
-        const int32_t pos = __ldg(a.group_pos + i);
-        pos_ok = pos >= 0 && int64_t(pos) < a.cs_rows;
-        const int col = 4 * ((K - 1) * 32 + lane);  // rope dims sit in the last column set
-        if (pos_ok && col >= kRopeStart) {
-            const int i0 = (col - kRopeStart) / 2;
-            const float *cs = a.cs + int64_t(pos) * kRopeD;
-            const float2 cc = __ldg(reinterpret_cast<const float2 *>(cs + i0));
-            const float2 sn = __ldg(reinterpret_cast<const float2 *>(cs + kRopeD / 2 + i0));
-            const float c2[2] = {cc.x, cc.y}, s2[2] = {sn.x, sn.y};
-#pragma unroll
-            for (int q = 0; q < 2; ++q) {
-                const float x0 = y[K - 1][2 * q], x1 = y[K - 1][2 * q + 1];
-                y[K - 1][2 * q] = __fsub_rn(__fmul_rn(x0, c2[q]), __fmul_rn(x1, s2[q]));
-                y[K - 1][2 * q + 1] = __fadd_rn(__fmul_rn(x0, s2[q]), __fmul_rn(x1, c2[q]));
-            }
-        }
-    }
-    const int64_t slot = __ldg(a.loc + i);
-    if (!pos_ok || slot < 0 || slot >= a.pool_slots) {
-        if (lane == 0) raise_err(a.err, pos_ok ? KVQ_DEVERR_SLOT : KVQ_DEVERR_POS);
-        return;
-    }
-    uint8_t *crow = PK::code_row(a.pool, slot);
-    uint8_t *srow = PK::scale_row(a.pool, slot);
-#pragma unroll
-    for (int k = 0; k < K; ++k) {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) y[k][e] = round_bf16(y[k][e]);
-        uint32_t am = max(max(abs_bits(y[k][0]), abs_bits(y[k][1])), max(abs_bits(y[k][2]), abs_bits(y[k][3])));
-#pragma unroll
-        for (int off = 1; off < 8; off <<= 1) am = max(am, __shfl_xor_sync(0xffffffffu, am, off));
-        const int colq = k * 32 + lane;  // float4 column: dims 4colq .. 4colq+3, block colq / 8
-        uint32_t sbyte;
-        if constexpr (L == Layout::V41) {
-            sbyte = v41_scale_byte(am);
-            const float mult = v41_multiplier(sbyte);
-            const uint32_t lo = cvt_e4m3x2(__fmul_rn(y[k][0], mult), __fmul_rn(y[k][1], mult));
-            const uint32_t hi = cvt_e4m3x2(__fmul_rn(y[k][2], mult), __fmul_rn(y[k][3], mult));
-            *reinterpret_cast<uint32_t *>(crow + 4 * colq) = lo | (hi << 16);
-        } else {
-            sbyte = fp4_scale_byte(am);
-            const float S = e4m3x2_to_f32x2(sbyte).x;
-            const float inv = __frcp_rn(S);
-            uint32_t word = 0;
-            if (S != 0.0f)
-                word = cvt_e2m1x2(__fmul_rn(y[k][0], inv), __fmul_rn(y[k][1], inv)) |
-                       (cvt_e2m1x2(__fmul_rn(y[k][2], inv), __fmul_rn(y[k][3], inv)) << 8);
-            *reinterpret_cast<uint16_t *>(crow + 2 * colq) = uint16_t(word);
-        }
-        if ((lane & 7) == 0) srow[colq >> 3] = uint8_t(sbyte);
-    }
-    if constexpr (T::kScaleBytes == 32) {
-        if (lane == 0) st_u4(srow + 16, make_uint4(0u, 0u, 0u, 0u));
-    }
-}
-
-template <Layout L, int PB, int R, bool RP>
-kvq_status launch_compress_decode(const DecodeArgs &a, cudaStream_t stream) {
-    const int64_t blocks = (a.n + kDecWarps - 1) / kDecWarps;
-    if (blocks > 0x7FFFFFFF) return KVQ_ERR_INVALID_ARG;
-    return launch_pdl(compress_decode_kernel<L, PB, R, RP>, dim3(unsigned(blocks)), dim3(kDecWarps * 32),
-                      stream, a);
-}
-
-template <typename F>
-kvq_status with_ratio(int r, F &&f) {
-    switch (r) {
-        case 1: return f(std::integral_constant<int, 1>{});
-        case 2: return f(std::integral_constant<int, 2>{});
-        case 4: return f(std::integral_constant<int, 4>{});
-        case 128: return f(std::integral_constant<int, 128>{});
-        default: return KVQ_ERR_UNSUPPORTED;
-    }
-}
-
 }  // namespace
 }  // namespace kvq
 
@@ -394,58 +221,6 @@ extern "C" kvq_status kvq_compress(kvq_layout layout, int page_bits, int ratio, 
                 return with_bool(rope, [&](auto RPc) {
                     return launch_compress<decltype(Lc)::value, decltype(PBc)::value,
                                            decltype(Rc)::value, decltype(RPc)::value>(a, s);
-                });
-            });
-        });
-    });
-}
-
-extern "C" kvq_status kvq_compress_decode(kvq_layout layout, int page_bits, int ratio, unsigned flags,
-                                          const float *values, const float *scores, int64_t n, float *state,
-                                          int32_t *count, const int32_t *req, int64_t n_state,
-                                          const float *cos_sin, int64_t cos_sin_rows, const int32_t *group_pos,
-                                          const int32_t *loc, uint8_t *pool, int64_t pool_slots, int32_t *err,
-                                          struct CUstream_st *stream) {
-    kvq_status st = check_pool(layout, page_bits, pool, pool_slots);
-    if (st != KVQ_OK) return st;
-    if (flags & ~unsigned(KVQ_FLAG_ROPE | KVQ_FLAG_NORM)) return KVQ_ERR_INVALID_ARG;
-    if (flags & KVQ_FLAG_NORM) return KVQ_ERR_UNSUPPORTED;
-    if (ratio < 1) return KVQ_ERR_INVALID_ARG;
-    if (ratio != 1 && ratio != 2 && ratio != 4 && ratio != 128) return KVQ_ERR_UNSUPPORTED;
-    if (n < 0 || n_state < 0) return KVQ_ERR_INVALID_ARG;
-    if (n == 0) return KVQ_OK;  // nothing to enqueue
-    if (!values || !scores || !aligned(values, 16) || !aligned(scores, 16)) return KVQ_ERR_INVALID_ARG;
-    if (!state || !aligned(state, 16) || !count || !aligned(count, 4) || n_state == 0) return KVQ_ERR_INVALID_ARG;
-    if (req && !aligned(req, 4)) return KVQ_ERR_INVALID_ARG;
-    if (!req && n > n_state) return KVQ_ERR_INVALID_ARG;
-    if (!loc || !aligned(loc, 4)) return KVQ_ERR_INVALID_ARG;
-    const bool rope = flags & KVQ_FLAG_ROPE;
-    if (rope && (!cos_sin || !aligned(cos_sin, 16) || cos_sin_rows <= 0 || !group_pos || !aligned(group_pos, 4)))
-        return KVQ_ERR_INVALID_ARG;
-    if (err && !aligned(err, 4)) return KVQ_ERR_INVALID_ARG;
-
-    DecodeArgs a;
-    a.values = values;
-    a.scores = scores;
-    a.n = n;
-    a.state = state;
-    a.count = count;
-    a.req = req;
-    a.n_state = n_state;
-    a.cs = cos_sin;
-    a.cs_rows = cos_sin_rows;
-    a.group_pos = group_pos;
-    a.loc = loc;
-    a.pool = pool;
-    a.pool_slots = pool_slots;
-    a.err = err;
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    return with_layout(layout, [&](auto Lc) {
-        return with_page_bits(page_bits, [&](auto PBc) {
-            return with_ratio(ratio, [&](auto Rc) {
-                return with_bool(rope, [&](auto RPc) {
-                    return launch_compress_decode<decltype(Lc)::value, decltype(PBc)::value,
-                                                  decltype(Rc)::value, decltype(RPc)::value>(a, s);
                 });
             });
         });

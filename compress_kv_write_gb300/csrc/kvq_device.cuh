@@ -299,6 +299,30 @@ __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
+// One fp32 float4 from a streamed (read-once) row.
+__device__ __forceinline__ float4 ld_f4(const float *p) {
+    uint4 r = ld_stream_u4(p);
+    return make_float4(__uint_as_float(r.x), __uint_as_float(r.y), __uint_as_float(r.z),
+                       __uint_as_float(r.w));
+}
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+// L2 prefetch hints.  They move lines into L2 only (never into L1 or
+// registers), and every write of any grid reaches L2, so issuing them before
+// griddepcontrol.wait cannot make a later load see stale data.
+// Bulk form: p 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void prefetch_l2_bulk(const void *p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void prefetch_l2(const void *p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+// Into this SM's L1 as well; issue it only after griddepcontrol.wait.
+__device__ __forceinline__ void prefetch_l1(const void *p) {
+    asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
+}
+
 __device__ __forceinline__ uint4 lds_u4(const void *p) {
     uint4 r;
     asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"

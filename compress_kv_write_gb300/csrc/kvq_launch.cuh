@@ -90,6 +90,18 @@ kvq_status with_page_bits(int pb, F &&f) {
     }
 }
 
+// Compressor ratios compiled in.
+template <typename F>
+kvq_status with_ratio(int r, F &&f) {
+    switch (r) {
+        case 1: return f(std::integral_constant<int, 1>{});
+        case 2: return f(std::integral_constant<int, 2>{});
+        case 4: return f(std::integral_constant<int, 4>{});
+        case 128: return f(std::integral_constant<int, 128>{});
+        default: return KVQ_ERR_UNSUPPORTED;
+    }
+}
+
 template <typename F>
 kvq_status with_layout(int layout, F &&f) {
     switch (layout) {

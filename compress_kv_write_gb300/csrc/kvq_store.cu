@@ -174,6 +174,14 @@ __global__ void __launch_bounds__(kStoreThreads) store_warp_kernel(const StoreAr
     const int64_t start = a.n * gw / W;
     const int cnt = int(a.n * (gw + 1) / W - start);
 
+    // While the upstream grid drains: pull this warp's first NS rows and its
+    // slot / position lines into L2 (hints only; the loads come after the wait).
+    if (lane < cnt && lane < NS) prefetch_l2_bulk(a.x + (start + lane) * a.row_stride_bytes, SM::XB);
+    if (lane == 0 && cnt > 0) {
+        prefetch_l2(kLoc64 ? static_cast<const void *>(static_cast<const int64_t *>(a.loc) + start)
+                           : static_cast<const void *>(static_cast<const int32_t *>(a.loc) + start));
+        if constexpr (kRope) prefetch_l2(a.pos + start);
+    }
     pdl_wait();
 
     // Slot / position of tokens 32b .. 32b+31 of this warp, one per lane,
@@ -267,11 +275,17 @@ __global__ void __launch_bounds__(kStoreThreads) store_warp_kernel(const StoreAr
         float cosv[E / 2], sinv[E / 2];
         if constexpr (kRope) {
             if (lane >= kRopeLane0) {
-                const float *cs = reinterpret_cast<const float *>(slot_sm + SM::XB + (lane - kRopeLane0) * E * 4);
-#pragma unroll
-                for (int q = 0; q < E / 2; ++q) {
-                    cosv[q] = cs[q];
-                    sinv[q] = cs[E / 2 + q];
+                const uint8_t *cs = slot_sm + SM::XB + (lane - kRopeLane0) * E * 4;
+                if constexpr (E == 8) {
+                    const uint4 c4 = lds_u4(cs), s4 = lds_u4(cs + 16);
+                    cosv[0] = __uint_as_float(c4.x), cosv[1] = __uint_as_float(c4.y);
+                    cosv[2] = __uint_as_float(c4.z), cosv[3] = __uint_as_float(c4.w);
+                    sinv[0] = __uint_as_float(s4.x), sinv[1] = __uint_as_float(s4.y);
+                    sinv[2] = __uint_as_float(s4.z), sinv[3] = __uint_as_float(s4.w);
+                } else {
+                    const float2 c2 = *reinterpret_cast<const float2 *>(cs);
+                    const float2 s2 = *reinterpret_cast<const float2 *>(cs + 8);
+                    cosv[0] = c2.x, cosv[1] = c2.y, sinv[0] = s2.x, sinv[1] = s2.y;
                 }
             }
         }
@@ -294,15 +308,18 @@ __global__ void __launch_bounds__(kStoreThreads) store_warp_kernel(const StoreAr
         for (int kk = 0; kk < K; ++kk) unpack_chunk<kBf16>(raw[kk], v[kk]);
 
         if constexpr (kNorm) {
-            float2 ss2 = make_float2(0.f, 0.f);
+            // four independent partial sums (short dependency chains)
+            float2 ss2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                             make_float2(0.f, 0.f)};
 #pragma unroll
             for (int kk = 0; kk < K; ++kk)
 #pragma unroll
                 for (int e = 0; e < E; e += 2) {
                     const float2 t = make_float2(v[kk][e], v[kk][e + 1]);
-                    ss2 = ffma2(t, t, ss2);
+                    const int j = (kk * E / 2 + e / 2) & 3;
+                    ss2[j] = ffma2(t, t, ss2[j]);
                 }
-            float ss = ss2.x + ss2.y;
+            float ss = ((ss2[0].x + ss2[0].y) + (ss2[1].x + ss2[1].y)) + ((ss2[2].x + ss2[2].y) + (ss2[3].x + ss2[3].y));
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
             const float ms = ss * (1.0f / kD);
@@ -328,7 +345,7 @@ __global__ void __launch_bounds__(kStoreThreads) store_warp_kernel(const StoreAr
                 }
             }
         }
-        if constexpr (kNorm || kRope) {
+        if constexpr (kNorm || (kRope && !kBf16)) {
 #pragma unroll
             for (int kk = 0; kk < K; ++kk)
 #pragma unroll
@@ -337,6 +354,16 @@ __global__ void __launch_bounds__(kStoreThreads) store_warp_kernel(const StoreAr
                     v[kk][e] = bf16_lo(b);
                     v[kk][e + 1] = bf16_hi(b);
                 }
+        } else if constexpr (kRope) {
+            // bf16 input, no norm: only the rotated values left the bf16 grid
+            if (lane >= kRopeLane0) {
+#pragma unroll
+                for (int e = 0; e < E; e += 2) {
+                    const uint32_t b = pack_bf16x2(v[K - 1][e], v[K - 1][e + 1]);
+                    v[K - 1][e] = bf16_lo(b);
+                    v[K - 1][e + 1] = bf16_hi(b);
+                }
+            }
         }
         encode_store<L, PageBits, E, K>(v, slot, a.pool, lane);
     }
@@ -385,6 +412,14 @@ __global__ void __launch_bounds__(kStoreThreads, 4) store_pair_kernel(const Stor
     const int cnt = int(a.n * (gw + 1) / W - start);
     const int npairs = (cnt + 1) >> 1;
 
+    // While the upstream grid drains: L2 hints for this warp's first NS pairs
+    // and its slot / position lines (the loads come after the wait).
+    if (lane < cnt && lane < 2 * NS) prefetch_l2_bulk(a.x + (start + lane) * a.row_stride_bytes, SM::XB);
+    if (lane == 0 && cnt > 0) {
+        prefetch_l2(kLoc64 ? static_cast<const void *>(static_cast<const int64_t *>(a.loc) + start)
+                           : static_cast<const void *>(static_cast<const int32_t *>(a.loc) + start));
+        if constexpr (kRope) prefetch_l2(a.pos + start);
+    }
     pdl_wait();
 
     if constexpr (kNorm) {  // the weight row, block-swizzled like fp32 rows
