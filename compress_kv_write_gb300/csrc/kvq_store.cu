@@ -83,17 +83,24 @@ struct WarpStoreSmem {
     static_assert(SLOT % 16 == 0 && kWarpBytes % 16 == 0, "16-byte aligned slots");
 };
 
-// Quantise one token held as v[K][E] (lane's chunks k*32 + lane) and write
-// its code row and scale row into slot `slot` (validated, < 2^31).  The lane
-// that leads a quant block writes that block's scale byte.
-template <Layout L, int PageBits, int E, int K>
-__device__ __forceinline__ void encode_store(float (&v)[K][E], int32_t slot, uint8_t *pool, int lane) {
-    constexpr int LPB = kBlock / E;
+// Code row and scale row of slot `slot` (validated, < 2^31).
+template <Layout L, int PageBits>
+__device__ __forceinline__ void row_ptrs(int32_t slot, uint8_t *pool, uint8_t *&crow, uint8_t *&srow) {
     using PK = PagedKV<L, PageBits>;
     using T = LayoutTraits<L>;
-    float am[K];
+    uint8_t *page = pool + int64_t(slot >> PageBits) * PK::kPageBytes;
+    const int row = slot & int(PK::kPage - 1);
+    crow = page + row * T::kCodeBytes;
+    srow = page + PK::kPage * T::kCodeBytes + row * T::kScaleBytes;
+}
+
+// Block absmax of chunks K0 .. K1-1 of one token held as v[K][E] (lane's
+// chunks k*32 + lane): a quant block spans kBlock / E adjacent lanes.
+template <int E, int K, int K0, int K1>
+__device__ __forceinline__ void block_amax(float (&v)[K][E], float (&am)[K]) {
+    constexpr int LPB = kBlock / E;
 #pragma unroll
-    for (int k = 0; k < K; ++k) {
+    for (int k = K0; k < K1; ++k) {
         float m[E / 2];
 #pragma unroll
         for (int e = 0; e < E / 2; ++e) m[e] = fmaxf(fabsf(v[k][2 * e]), fabsf(v[k][2 * e + 1]));
@@ -106,12 +113,16 @@ __device__ __forceinline__ void encode_store(float (&v)[K][E], int32_t slot, uin
         for (int off = 1; off < LPB; off <<= 1) mm = fmaxf(mm, __shfl_xor_sync(0xffffffffu, mm, off));
         am[k] = mm;
     }
-    const int64_t page = int64_t(slot >> PageBits) * PK::kPageBytes;
-    const int row = slot & int(PK::kPage - 1);
-    uint8_t *crow = pool + page + row * T::kCodeBytes;
-    uint8_t *srow = pool + page + PK::kPage * T::kCodeBytes + row * T::kScaleBytes;
+}
+
+// Quantise chunks K0 .. K1-1 with their block absmax into the token's code
+// row and scale row.  The lane that leads a quant block writes its scale byte.
+template <Layout L, int E, int K, int K0, int K1>
+__device__ __forceinline__ void quant_store(float (&v)[K][E], const float (&am)[K], uint8_t *crow, uint8_t *srow,
+                                            int lane) {
+    constexpr int LPB = kBlock / E;
 #pragma unroll
-    for (int k = 0; k < K; ++k) {
+    for (int k = K0; k < K1; ++k) {
         const int c = k * 32 + lane;  // chunk index in the row
         uint32_t sbyte;
         if constexpr (L == Layout::V41) {
@@ -149,9 +160,22 @@ __device__ __forceinline__ void encode_store(float (&v)[K][E], int32_t slot, uin
         }
         if (lane % LPB == 0) srow[c / LPB] = uint8_t(sbyte);
     }
-    if constexpr (T::kScaleBytes == 32) {
+    if constexpr (LayoutTraits<L>::kScaleBytes == 32 && K1 == K) {
         if (lane == 0) st_u4(srow + 16, make_uint4(0u, 0u, 0u, 0u));
     }
+}
+
+// Round v[k] to bf16 (ties to even), in place, for chunks K0 .. K1-1.
+template <int E, int K, int K0, int K1>
+__device__ __forceinline__ void round_chunks(float (&v)[K][E]) {
+#pragma unroll
+    for (int kk = K0; kk < K1; ++kk)
+#pragma unroll
+        for (int e = 0; e < E; e += 2) {
+            const uint32_t b = pack_bf16x2(v[kk][e], v[kk][e + 1]);
+            v[kk][e] = bf16_lo(b);
+            v[kk][e + 1] = bf16_hi(b);
+        }
 }
 
 template <Layout L, int PageBits, bool kBf16, bool kLoc64, bool kNorm, bool kRope>
@@ -206,7 +230,9 @@ __global__ void __launch_bounds__(kStoreThreads) store_warp_kernel(const StoreAr
     }
     int cur_b = 0;
 
-    // copies of token j into the next ring slot; one commit group per token
+    // Copies of token j into the next ring slot: one commit group for the
+    // row and, with RoPE, a second one for its cos/sin values (which wait on
+    // the position), so the rest of the row can be finished while they land.
     const uint8_t *src_next = a.x + start * a.row_stride_bytes + lane * 16;
     int ring_in = 0;
     auto issue = [&](int j) {
@@ -215,6 +241,7 @@ __global__ void __launch_bounds__(kStoreThreads) store_warp_kernel(const StoreAr
 #pragma unroll
             for (int k = 0; k < K; ++k) cp_async16(slot + k * 512, src_next + k * 512);
             if constexpr (kRope) {
+                cp_async_commit();
                 const int32_t pj = __shfl_sync(0xffffffffu, (j >> 5) == cur_b ? p_cur : p_nxt, j & 31);
                 if (lane >= kRopeLane0 && pj >= 0) {
                     const int i0 = ((K - 1) * 32 + lane) * E / 2 - kRopeStart / 2;
@@ -231,9 +258,13 @@ __global__ void __launch_bounds__(kStoreThreads) store_warp_kernel(const StoreAr
             }
             src_next += a.row_stride_bytes;
             ring_in = (ring_in + 1) & (NS - 1);
+        } else if constexpr (kRope) {
+            cp_async_commit();  // keep two groups per token
         }
         cp_async_commit();
     };
+    // groups committed per token, and the waits for token k's row and cos/sin
+    constexpr int kGroups = kRope ? 2 : 1;
 
     float wreg[K][E];
     if constexpr (kNorm) {
@@ -266,29 +297,13 @@ __global__ void __launch_bounds__(kStoreThreads) store_warp_kernel(const StoreAr
                 if constexpr (kRope) p_nxt = ld_pos(k + 32 + lane);
             }
         }
-        cp_async_wait<D - 1>();  // this lane's copies of token k have landed
+        // Token k's row has landed once at most kGroups * D - 1 groups are pending.
+        cp_async_wait<kGroups * D - 1>();
         const uint8_t *slot_sm = wsm + ring_out * SM::SLOT;
         ring_out = (ring_out + 1) & (NS - 1);
         uint4 raw[K];
 #pragma unroll
         for (int kk = 0; kk < K; ++kk) raw[kk] = lds_u4(slot_sm + (kk * 32 + lane) * 16);
-        float cosv[E / 2], sinv[E / 2];
-        if constexpr (kRope) {
-            if (lane >= kRopeLane0) {
-                const uint8_t *cs = slot_sm + SM::XB + (lane - kRopeLane0) * E * 4;
-                if constexpr (E == 8) {
-                    const uint4 c4 = lds_u4(cs), s4 = lds_u4(cs + 16);
-                    cosv[0] = __uint_as_float(c4.x), cosv[1] = __uint_as_float(c4.y);
-                    cosv[2] = __uint_as_float(c4.z), cosv[3] = __uint_as_float(c4.w);
-                    sinv[0] = __uint_as_float(s4.x), sinv[1] = __uint_as_float(s4.y);
-                    sinv[2] = __uint_as_float(s4.z), sinv[3] = __uint_as_float(s4.w);
-                } else {
-                    const float2 c2 = *reinterpret_cast<const float2 *>(cs);
-                    const float2 s2 = *reinterpret_cast<const float2 *>(cs + 8);
-                    cosv[0] = c2.x, cosv[1] = c2.y, sinv[0] = s2.x, sinv[1] = s2.y;
-                }
-            }
-        }
         const int32_t slot = __shfl_sync(0xffffffffu, sl_cur, k & 31);
         int32_t pk = 0;
         if constexpr (kRope) pk = __shfl_sync(0xffffffffu, p_cur, k & 31);
@@ -334,8 +349,30 @@ __global__ void __launch_bounds__(kStoreThreads) store_warp_kernel(const StoreAr
                     v[kk][e + 1] = t.y;
                 }
         }
+        uint8_t *crow, *srow;
+        float am[K];
         if constexpr (kRope) {
+            // Chunks before the rotated one are final: round and store them
+            // while this token's cos/sin copies land.
+            if constexpr (kNorm || !kBf16) round_chunks<E, K, 0, K - 1>(v);
+            block_amax<E, K, 0, K - 1>(v, am);
+            row_ptrs<L, PageBits>(slot, a.pool, crow, srow);
+            quant_store<L, E, K, 0, K - 1>(v, am, crow, srow, lane);
+            cp_async_wait<2 * D>();  // ... and its cos/sin values (two groups were added since)
             if (lane >= kRopeLane0) {
+                float cosv[E / 2], sinv[E / 2];
+                const uint8_t *cs = slot_sm + SM::XB + (lane - kRopeLane0) * E * 4;
+                if constexpr (E == 8) {
+                    const uint4 c4 = lds_u4(cs), s4 = lds_u4(cs + 16);
+                    cosv[0] = __uint_as_float(c4.x), cosv[1] = __uint_as_float(c4.y);
+                    cosv[2] = __uint_as_float(c4.z), cosv[3] = __uint_as_float(c4.w);
+                    sinv[0] = __uint_as_float(s4.x), sinv[1] = __uint_as_float(s4.y);
+                    sinv[2] = __uint_as_float(s4.z), sinv[3] = __uint_as_float(s4.w);
+                } else {
+                    const float2 c2 = *reinterpret_cast<const float2 *>(cs);
+                    const float2 s2 = *reinterpret_cast<const float2 *>(cs + 8);
+                    cosv[0] = c2.x, cosv[1] = c2.y, sinv[0] = s2.x, sinv[1] = s2.y;
+                }
 #pragma unroll
                 for (int q = 0; q < E / 2; ++q) {
                     const float x0 = v[K - 1][2 * q], x1 = v[K - 1][2 * q + 1];
@@ -343,29 +380,18 @@ __global__ void __launch_bounds__(kStoreThreads) store_warp_kernel(const StoreAr
                     v[K - 1][2 * q] = __fsub_rn(__fmul_rn(x0, c), __fmul_rn(x1, sn));
                     v[K - 1][2 * q + 1] = __fadd_rn(__fmul_rn(x0, sn), __fmul_rn(x1, c));
                 }
+                // bf16 input without norm: only the rotated values left the bf16 grid
+                if constexpr (!kNorm && kBf16) round_chunks<E, K, K - 1, K>(v);
             }
+            if constexpr (kNorm || !kBf16) round_chunks<E, K, K - 1, K>(v);
+            block_amax<E, K, K - 1, K>(v, am);
+            quant_store<L, E, K, K - 1, K>(v, am, crow, srow, lane);
+        } else {
+            if constexpr (kNorm) round_chunks<E, K, 0, K>(v);
+            block_amax<E, K, 0, K>(v, am);
+            row_ptrs<L, PageBits>(slot, a.pool, crow, srow);
+            quant_store<L, E, K, 0, K>(v, am, crow, srow, lane);
         }
-        if constexpr (kNorm || (kRope && !kBf16)) {
-#pragma unroll
-            for (int kk = 0; kk < K; ++kk)
-#pragma unroll
-                for (int e = 0; e < E; e += 2) {
-                    const uint32_t b = pack_bf16x2(v[kk][e], v[kk][e + 1]);
-                    v[kk][e] = bf16_lo(b);
-                    v[kk][e + 1] = bf16_hi(b);
-                }
-        } else if constexpr (kRope) {
-            // bf16 input, no norm: only the rotated values left the bf16 grid
-            if (lane >= kRopeLane0) {
-#pragma unroll
-                for (int e = 0; e < E; e += 2) {
-                    const uint32_t b = pack_bf16x2(v[K - 1][e], v[K - 1][e + 1]);
-                    v[K - 1][e] = bf16_lo(b);
-                    v[K - 1][e + 1] = bf16_hi(b);
-                }
-            }
-        }
-        encode_store<L, PageBits, E, K>(v, slot, a.pool, lane);
     }
     cp_async_wait<0>();
 }
