@@ -670,16 +670,26 @@ def traffic_from_profiles(workload):
     return None
 
 
+def _code_only(text):
+    """C++ source without comments and with whitespace runs collapsed, so that
+    editing a comment does not count as changing a kernel."""
+    import re
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_source_sha(workload):
-    """Hash of the dominant kernel's translation unit and the shared headers."""
+    """Hash of the code (comments dropped) of the dominant kernel's translation
+    unit and the shared headers."""
     import hashlib
     h = hashlib.sha256()
     d = os.path.join(ROOT, "compress_kv_write_gb300", "csrc")
     files = [KERNEL_SOURCES[SPECS[workload]["kind"]], "kvq_device.cuh", "kvq_launch.cuh"]
     for fn in files:
-        with open(os.path.join(d, fn), "rb") as f:
+        with open(os.path.join(d, fn), encoding="utf-8") as f:
             h.update(fn.encode())
-            h.update(f.read())
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

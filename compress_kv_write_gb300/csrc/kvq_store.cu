@@ -6,7 +6,10 @@
 // Both kernels are persistent (as many CTAs of four warps as are resident at
 // once); warp w of W owns the contiguous token range [n*w/W, n*(w+1)/W) and
 // keeps its next rows in flight in a per-warp shared-memory ring filled with
-// cp.async (one commit group per ring slot).  Slot indices and positions of
+// cp.async (one commit group per ring slot; the V41 kernel with RoPE commits
+// a token's cos/sin values as a second group, so that everything but the
+// rotated chunk is finished while they land).  Before the PDL wait each warp
+// prefetches its first rows into L2.  Slot indices and positions of
 // 32 tokens sit one per lane, validated once, and are fetched with a
 // shuffle.  Math is fp32; the products of the RMSNorm and of the rotation are
 // rounded one by one, as in the definition.

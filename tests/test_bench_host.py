@@ -58,3 +58,11 @@ def test_reference_arm_json(name, monkeypatch):
 def test_warmup_floor():
     with pytest.raises(SystemExit):
         bench.main(["--impl", "reference", "--warmup", "2"])
+
+
+def test_source_hash_ignores_comments_only():
+    a = "int f(int x) {  // doubles\n  return 2 * x; /* no overflow\n check */ }\n"
+    b = "int f(int x) {\n  // a different comment\n  return 2 * x;\n}\n"
+    c = "int f(int x) { return 3 * x; }"
+    assert bench._code_only(a) == bench._code_only(b)
+    assert bench._code_only(a) != bench._code_only(c)
