@@ -683,3 +683,79 @@ def test_compress_decode_bad_state_index(K):
     assert err.item() == K.kvq.DEVERR_STATE
     assert count.cpu().tolist() == [1, 7]
     assert int(pool.sum().item()) == 0
+
+
+# --------------------------------------------------------------------------- strided rows
+
+@pytest.mark.parametrize("layout", [1, 2])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("flags", [0, 1, 3])
+def test_store_strided_rows(K, layout, dtype, flags):
+    """x is the K slice of a wider projection: 512 columns at a 128-byte offset
+    inside wider rows (x_row_stride > 512).  The pool must hold the bytes the
+    oracle writes from the contiguous copy of the same rows."""
+    from compress_kv_write_gb300 import synth
+    n, slots = 300, 1024
+    seed = 900 + layout * 10 + flags
+    xc = synth.store_rows_bf16(n, "cpu", seed)
+    if dtype == "f32":
+        xc = xc.float() * 1.25
+    pad = 128 // xc.element_size()
+    wide = torch.zeros((n, 512 + 3 * pad), dtype=xc.dtype)
+    wide[:, pad:pad + 512] = xc
+    x = wide.to(DEV)[:, pad:pad + 512]
+    assert x.stride(0) == 512 + 3 * pad and not x.is_contiguous()
+    loc = synth.injective_slots(n, slots, "cpu", seed)
+    w = synth.norm_weight("cpu", seed)
+    cs = synth.rope_table(4096, "cpu")
+    pos = synth.positions(n, "cpu", seed, max_pos=4096)
+    x_np = xc.numpy() if dtype == "f32" else _bf16_np(xc)
+    pool_o = np.zeros(slots * O.bytes_per_token(layout), np.uint8)
+    assert O.store(layout, 6, flags, x_np, loc.numpy(), pool_o, norm_weight=w.numpy(), eps=1e-6,
+                   cos_sin=cs.numpy(), pos=pos.numpy()) == O.OK
+    pool = torch.zeros(slots * O.bytes_per_token(layout), dtype=torch.uint8, device=DEV)
+    err = _err(K)
+    K.kvq_store(layout, 6, flags, x, loc.to(DEV), pool, slots,
+                norm_weight=w.to(DEV) if flags & 2 else None, eps=1e-6,
+                cos_sin=cs.to(DEV) if flags & 1 else None, pos=pos.to(DEV) if flags & 1 else None, err=err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    got = np_u8(pool)
+    if flags & 2 == 0:
+        assert (got == pool_o).all()
+    else:
+        g = gather_rows(got, layout, 6, loc.numpy())
+        o = gather_rows(pool_o, layout, 6, loc.numpy())
+        y = np.stack([O.token_prequant(flags, x_np[t], w.numpy(), 1e-6, cs.numpy()[pos[t]]) for t in range(n)])
+        check_tolerance(layout, g[0], g[1], o[0], o[1], y)
+
+
+@pytest.mark.parametrize("layout", [1, 2])
+def test_dequant_into_strided_workspace(K, layout):
+    """Both dequants write into 512 columns of a wider bf16 workspace; the
+    columns around them stay untouched."""
+    from compress_kv_write_gb300 import synth
+    slots, n = 256, 256
+    x = synth.store_rows_bf16(n, "cpu", 31)
+    loc = synth.injective_slots(n, slots, "cpu", 31)
+    pool_o = np.zeros(slots * O.bytes_per_token(layout), np.uint8)
+    assert O.store(layout, 6, 0, _bf16_np(x), loc.numpy(), pool_o) == O.OK
+    pool = torch.from_numpy(pool_o).to(DEV)
+    pt = synth.page_table_perm(4, "cpu", 31)
+    rc, ws_o = O.dequant(layout, 6, pool_o, pt.numpy(), slots)
+    assert rc == O.OK
+    sel = torch.tensor([3, -1, 200, 77, 0, 255], dtype=torch.int64)
+    rc, sel_o = O.dequant_slots(layout, pool_o, sel.numpy())
+    assert rc == O.OK
+    sentinel = torch.tensor([0x7E11], dtype=torch.int16).view(torch.bfloat16)
+    for out_rows, run, ref in ((slots, lambda o, e: K.kvq_dequant(layout, 6, pool, 4, pt.to(DEV), o, err=e), ws_o),
+                               (6, lambda o, e: K.kvq_dequant_slots(layout, 6, pool, slots, sel.to(DEV), o, err=e),
+                                sel_o)):
+        wide = sentinel.expand(out_rows, 512 + 3 * 64).contiguous().to(DEV)
+        err = _err(K)
+        run(wide[:, 64:576], err)
+        torch.cuda.synchronize()
+        assert err.item() == 0
+        w16 = wide.cpu().view(torch.int16).numpy().view(np.uint16)
+        assert (w16[:, 64:576] == ref).all()
+        assert (w16[:, :64] == 0x7E11).all() and (w16[:, 576:] == 0x7E11).all()
