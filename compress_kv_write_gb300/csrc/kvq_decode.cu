@@ -196,7 +196,7 @@ kvq_status launch_compress_decode(DecodeArgs a, cudaStream_t stream) {
     const int64_t blocks = (a.n + kDecWarps - 1) / kDecWarps;
     if (blocks > 0x7FFFFFFF) return KVQ_ERR_INVALID_ARG;
     int64_t wave = 0;
-    const kvq_status st = resident_grid<compress_decode_kernel<L, PB, R, RP>>(kDecWarps * 32, 0, &wave);
+    const kvq_status st = resident_grid<compress_decode_kernel<L, PB, R, RP>, kDecWarps * 32>(0, &wave);
     if (st != KVQ_OK) return st;
     // Beyond one wave the hints would only duplicate the loads of CTAs that
     // start after the upstream grid has finished.

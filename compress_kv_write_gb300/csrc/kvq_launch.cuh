@@ -43,13 +43,15 @@ kvq_status launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, cudaStrea
     return launch_pdl_smem(kernel, grid, block, 0, stream, std::forward<Args>(args)...);
 }
 
-// Per-device launch limits of a kernel instance: opts it into `smem` bytes of
-// dynamic shared memory (once per device) and returns the largest grid that
-// is resident at once (blocks per SM x SMs).
+// Per-device launch limits of a kernel instance launched with CTAs of
+// `Threads` threads: opts it into `smem` bytes of dynamic shared memory (once
+// per device) and returns the largest grid that is resident at once (blocks
+// per SM x SMs).
 constexpr int kMaxDevices = 64;
 
-template <auto Kernel>
-kvq_status resident_grid(int threads, size_t smem, int64_t *grid_cap) {
+template <auto Kernel, int Threads>
+kvq_status resident_grid(size_t smem, int64_t *grid_cap) {
+    constexpr int threads = Threads;
     static std::atomic<int> cap[kMaxDevices];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
