@@ -5,8 +5,11 @@
 A step is one pass of the write path over one batch of synthetic input.  The
 default workload is the fused K RMSNorm + RoPE + V41 store of 16384 bf16 rows
 into a 2^20-slot paged pool (the largest batch of the store sweep); other
-workloads (--workload) cover the FP4 store, the full-pool dequant, the
-translated C4A compressor and the mixed C128A compressor.
+workloads (--workload) cover the plain and RoPE V41 stores, the FP4 store,
+the full-pool and selected-slot dequants, the translated C4A compressor, the
+mixed C128A compressor (both layouts), the decode-time C4A compressor, a
+61-layer step behind one translation (with the per-layer form timed beside
+it), and `sweep`, a hot-L2 latency table at bs 1 / 8 / 64 / 512.
 
 The timed region replays CUDA graphs holding exactly K steps (captured
 launches of the C ABI), bracketed by a barrier and a synchronize, timed with

@@ -4,7 +4,9 @@
 // (section 1 store_row, and the store-latency table).
 //
 // Both kernels are persistent (as many CTAs of four warps as are resident at
-// once); warp w of W owns the contiguous token range [n*w/W, n*(w+1)/W) and
+// once; the fused norm + RoPE V41 instance switches to one-warp CTAs from
+// three tokens per resident warp up); warp w of W owns the contiguous token
+// range [n*w/W, n*(w+1)/W) and
 // keeps its next rows in flight in a per-warp shared-memory ring filled with
 // cp.async (one commit group per ring slot; the V41 kernel with RoPE commits
 // a token's cos/sin values as a second group, so that everything but the
