@@ -189,7 +189,7 @@ class StoreWorkload(Workload):
         payload = 528 if self.layout == 1 else 272
         per = row_bytes + 8 + payload + ((4 + 256) if self.flags & 1 else 0)
         self.bytes_total = self.bytes_dominant = bs * per
-        self.dominant = "store_kernel"
+        self.dominant = "store_warp_kernel" if self.layout == 1 else "store_pair_kernel"
         total = self.R * bs * (row_bytes + 12)
         self.config["l2"] = (f"rotating {self.R} input sets ({total / 2**20:.0f} MB > 129 MB L2)"
                              if total > L2_BYTES else
@@ -516,7 +516,7 @@ class LayersWorkload(Workload):
         per_store = self.bs * B_STORE_ROPE
         self.bytes_dominant = per_store
         self.bytes_total = self.L * per_store + self.bs * B_TRANSLATE
-        self.dominant = "store_kernel"
+        self.dominant = "store_warp_kernel"
         self.config["l2"] = (f"rotating {self.R} step input sets ({self.R * per_set / 2**20:.0f} MB) "
                              f"over {self.L} pools of {self.swa_slots * 528 / 2**20:.0f} MB")
 
