@@ -51,7 +51,7 @@ def b_compress(r, payload=528):
 
 DEFAULT_STEPS = {
     "store_norm_rope": 200000, "store_rope": 200000, "store": 200000, "small": 200000,
-    "fp4_store": 20000, "fp4_dequant": 3000, "c4a": 20000, "c128a": 1000, "c128a_fp4": 1000,
+    "fp4_store": 20000, "fp4_store_16k": 200000, "fp4_dequant": 3000, "c4a": 20000, "c128a": 1000, "c128a_fp4": 1000,
     "layers": 2000, "dequant_select": 3000, "c4a_decode": 20000,
 }
 
@@ -62,6 +62,7 @@ SPECS = {
     "store_rope": dict(kind="store", flags=1, bs=16384, pool_slots=1 << 20, layout=1),
     "store_norm_rope": dict(kind="store", flags=3, bs=16384, pool_slots=1 << 20, layout=1),
     "fp4_store": dict(kind="store", flags=0, bs=262144, pool_slots=1 << 21, layout=2, student_t=True),
+    "fp4_store_16k": dict(kind="store", flags=0, bs=16384, pool_slots=1 << 21, layout=2, student_t=True),
     "fp4_dequant": dict(kind="dequant", pool_slots=1 << 21, layout=2),
     # decode-time C4A: one new row per request per step, the open group's softmax carried as state
     "c4a_decode": dict(kind="decode", ratio=4, layout=1, requests=16384, pool_slots=1 << 17,

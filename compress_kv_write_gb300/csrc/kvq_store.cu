@@ -519,9 +519,20 @@ __global__ void __launch_bounds__(kStoreThreads, 4) store_pair_kernel(const Stor
         cp_async_commit();
     };
 
+    if (npairs > 1) {
+        // The first pair lands before the next ones are requested: every warp
+        // starts at once, and the first pair is what holds it up (FP4 store
+        // at 16384 tokens: 5.07 -> 4.82 us).
+        issue(0);
+        pdl_trigger();
+        cp_async_wait<0>();
 #pragma unroll
-    for (int p = 0; p < D; ++p) issue(p);
-    pdl_trigger();
+        for (int p = 1; p < D; ++p) issue(p);
+    } else {
+#pragma unroll
+        for (int p = 0; p < D; ++p) issue(p);
+        pdl_trigger();
+    }
 
     int ring_out = 0;
     for (int k = 0; k < npairs; ++k) {
