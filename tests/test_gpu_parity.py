@@ -759,3 +759,38 @@ def test_dequant_into_strided_workspace(K, layout):
         w16 = wide.cpu().view(torch.int16).numpy().view(np.uint16)
         assert (w16[:, 64:576] == ref).all()
         assert (w16[:, :64] == 0x7E11).all() and (w16[:, 576:] == 0x7E11).all()
+
+
+@pytest.mark.parametrize("flags", [0, 1, 3])
+def test_store_many_tokens_per_warp(K, flags):
+    """262144 V41 tokens: every warp of the persistent grid holds more than 32
+    tokens, so the per-lane slot / position batches are reloaded inside the
+    loop; the whole pool must match the oracle."""
+    from compress_kv_write_gb300 import synth
+    n, slots = 1 << 18, 1 << 20
+    x = synth.store_rows_bf16(n, DEV, 7)
+    loc = synth.injective_slots(n, slots, DEV, 7)
+    pos = synth.positions(n, DEV, 7)
+    cs = synth.rope_table(65536, DEV)
+    w = synth.norm_weight(DEV, 7)
+    pool = torch.zeros(slots * 528, dtype=torch.uint8, device=DEV)
+    err = _err(K)
+    K.kvq_store(K.V41, 6, flags, x, loc, pool, slots, norm_weight=w, eps=1e-6, cos_sin=cs, pos=pos, err=err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    x_np, loc_np, pos_np = _bf16_np(x), loc.cpu().numpy(), pos.cpu().numpy()
+    cs_np, w_np = cs.cpu().numpy(), w.cpu().numpy()
+    pool_o = np.zeros(slots * 528, np.uint8)
+    assert O.store(O.V41, 6, flags, x_np, loc_np, pool_o, norm_weight=w_np, eps=1e-6, cos_sin=cs_np,
+                   pos=pos_np) == O.OK
+    got = np_u8(pool)
+    if flags & 2 == 0:
+        assert (got == pool_o).all()
+    else:
+        g = gather_rows(got, O.V41, 6, loc_np)
+        o = gather_rows(pool_o, O.V41, 6, loc_np)
+        sel = np.arange(0, n, 61)  # the prequant reference for a sample of the rows
+        y = np.stack([O.token_prequant(flags, x_np[t], w_np, 1e-6, cs_np[pos_np[t]]) for t in sel])
+        check_tolerance(O.V41, g[0][sel], g[1][sel], o[0][sel], o[1][sel], y)
+        diff = (g[0] != o[0]).mean()
+        assert diff < 1e-3, diff  # code bytes that differ anywhere in the batch
