@@ -794,3 +794,46 @@ def test_store_many_tokens_per_warp(K, flags):
         check_tolerance(O.V41, g[0][sel], g[1][sel], o[0][sel], o[1][sel], y)
         diff = (g[0] != o[0]).mean()
         assert diff < 1e-3, diff  # code bytes that differ anywhere in the batch
+
+
+# --------------------------------------------------------------------------- hand-worked blocks
+
+def test_kernels_reproduce_handworked_blocks(K):
+    """Every hand-worked block of tests/golden, stored by the CUDA store kernels
+    (fp32 input, no fused math) in quant blocks 0, 9 and 15 of its own token:
+    the code and scale bytes must be the hand-derived ones, and the paged
+    dequant must give the hand-derived values."""
+    from golden_io import load_blocks
+    for layout, fname in ((O.V41, "v41_blocks.txt"), (O.FP4, "fp4_blocks.txt")):
+        cases = load_blocks(fname)
+        blocks = (0, 9, 15)
+        n = len(cases) * len(blocks)
+        x = np.zeros((n, 512), np.float32)
+        for ci, (_, vals, _, _, _) in enumerate(cases):
+            for bi, blk in enumerate(blocks):
+                x[ci * len(blocks) + bi, blk * 32:(blk + 1) * 32] = vals
+        slots = max(64, -(-n // 64) * 64)
+        pool = torch.zeros(slots * O.bytes_per_token(layout), dtype=torch.uint8, device=DEV)
+        loc = torch.arange(n, dtype=torch.int64, device=DEV)
+        err = _err(K)
+        K.kvq_store(layout, 6, 0, torch.from_numpy(x).to(DEV), loc, pool, slots, err=err)
+        out = torch.empty((slots, 512), dtype=torch.bfloat16, device=DEV)
+        K.kvq_dequant(layout, 6, pool, slots // 64, torch.arange(slots // 64, dtype=torch.int32, device=DEV),
+                      out, err=err)
+        torch.cuda.synchronize()
+        assert err.item() == 0
+        codes, scales = gather_rows(np_u8(pool), layout, 6, np.arange(n))
+        deq = out.float().cpu().numpy()
+        cpb = 32 if layout == O.V41 else 16          # code bytes per quant block
+        for ci, (name, _, scale, cbytes, dvals) in enumerate(cases):
+            for bi, blk in enumerate(blocks):
+                t = ci * len(blocks) + bi
+                assert scales[t, blk] == scale, (name, blk)
+                assert (np.delete(scales[t, :16], blk) == 0).all(), name
+                if layout == O.FP4:
+                    assert (scales[t, 16:] == 0).all(), name
+                cb = codes[t, blk * cpb:(blk + 1) * cpb]
+                for j in range(cpb):
+                    assert cb[j] == cbytes.get(j, 0x00), (name, blk, j, hex(cb[j]))
+                for i, v in dvals.items():
+                    assert deq[t, blk * 32 + i] == np.float32(v), (name, blk, i, deq[t, blk * 32 + i], v)
