@@ -837,3 +837,52 @@ def test_kernels_reproduce_handworked_blocks(K):
                     assert cb[j] == cbytes.get(j, 0x00), (name, blk, j, hex(cb[j]))
                 for i, v in dvals.items():
                     assert deq[t, blk * 32 + i] == np.float32(v), (name, blk, i, deq[t, blk * 32 + i], v)
+
+
+@pytest.mark.parametrize("flags", [0, 1, 3])
+def test_bad_rows_in_a_large_batch(K, flags):
+    """20000 V41 tokens (several per warp, so the staggered first copy and, for
+    norm + RoPE, the one-warp CTAs are in play) with out-of-range slots and
+    positions scattered through the batch: the error word carries the flags,
+    the bad rows write nothing and every other row matches the oracle."""
+    from compress_kv_write_gb300 import synth
+    n, slots = 20000, 1 << 16
+    x = synth.store_rows_bf16(n, "cpu", 11)
+    loc = synth.injective_slots(n, slots, "cpu", 11)
+    pos = synth.positions(n, "cpu", 11, max_pos=4096)
+    bad_slot = np.arange(17, n, 997)
+    loc[bad_slot[0::2]] = slots          # one past the end
+    loc[bad_slot[1::2]] = -3
+    bad_pos = np.arange(500, n, 1511) if flags & 1 else np.array([], np.int64)
+    pos[bad_pos] = 4096                  # one past the table
+    cs = synth.rope_table(4096, "cpu")
+    w = synth.norm_weight("cpu", 11)
+    pool = torch.zeros(slots * 528, dtype=torch.uint8, device=DEV)
+    err = _err(K)
+    K.kvq_store(K.V41, 6, flags, x.to(DEV), loc.to(DEV), pool, slots, norm_weight=w.to(DEV), eps=1e-6,
+                cos_sin=cs.to(DEV), pos=pos.to(DEV), err=err)
+    torch.cuda.synchronize()
+    want = K.kvq.DEVERR_SLOT | (K.kvq.DEVERR_POS if flags & 1 else 0)
+    assert err.item() == want
+    good = np.setdiff1d(np.arange(n), np.union1d(bad_slot, bad_pos))
+    x_np = _bf16_np(x)
+    pool_o = np.zeros(slots * 528, np.uint8)
+    assert O.store(O.V41, 6, flags, x_np[good], loc.numpy()[good], pool_o, norm_weight=w.numpy(), eps=1e-6,
+                   cos_sin=cs.numpy(), pos=pos.numpy()[good]) == O.OK
+    got = np_u8(pool)
+    if flags & 2 == 0:
+        assert (got == pool_o).all()
+    else:
+        g = gather_rows(got, O.V41, 6, loc.numpy()[good])
+        o = gather_rows(pool_o, O.V41, 6, loc.numpy()[good])
+        assert (g[0] != o[0]).mean() < 1e-3
+        sel = good[::37]
+        gs = gather_rows(got, O.V41, 6, loc.numpy()[sel])
+        os_ = gather_rows(pool_o, O.V41, 6, loc.numpy()[sel])
+        y = np.stack([O.token_prequant(flags, x_np[t], w.numpy(), 1e-6, cs.numpy()[pos[t]]) for t in sel])
+        check_tolerance(O.V41, gs[0], gs[1], os_[0], os_[1], y)
+        # nothing outside the good rows' slots was written
+        mask = np.zeros(slots, bool)
+        mask[loc.numpy()[good]] = True
+        cz, sz = gather_rows(got, O.V41, 6, np.flatnonzero(~mask))
+        assert (cz == 0).all() and (sz == 0).all()
