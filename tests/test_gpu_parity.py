@@ -886,3 +886,32 @@ def test_bad_rows_in_a_large_batch(K, flags):
         mask[loc.numpy()[good]] = True
         cz, sz = gather_rows(got, O.V41, 6, np.flatnonzero(~mask))
         assert (cz == 0).all() and (sz == 0).all()
+
+
+@pytest.mark.parametrize("flags", [0, 1])
+def test_fp4_bad_rows_in_a_large_batch(K, flags):
+    """The FP4 pair kernel on 20000 tokens (several pairs per warp, so the
+    staggered first copy is in play) with out-of-range slots and positions:
+    flagged, skipped, and every other row bit-exact to the oracle."""
+    from compress_kv_write_gb300 import synth
+    n, slots = 20000, 1 << 16
+    bpt = O.bytes_per_token(O.FP4)
+    x = synth.student_t_rows_bf16(n, "cpu", 13)
+    loc = synth.injective_slots(n, slots, "cpu", 13)
+    pos = synth.positions(n, "cpu", 13, max_pos=4096)
+    bad_slot = np.arange(29, n, 1009)
+    loc[bad_slot] = slots + 5
+    bad_pos = np.arange(300, n, 1213) if flags & 1 else np.array([], np.int64)
+    pos[bad_pos] = -1
+    cs = synth.rope_table(4096, "cpu")
+    pool = torch.zeros(slots * bpt, dtype=torch.uint8, device=DEV)
+    err = _err(K)
+    K.kvq_store(K.V41_FP4, 6, flags, x.to(DEV), loc.to(DEV), pool, slots, cos_sin=cs.to(DEV), pos=pos.to(DEV),
+                err=err)
+    torch.cuda.synchronize()
+    assert err.item() == K.kvq.DEVERR_SLOT | (K.kvq.DEVERR_POS if flags & 1 else 0)
+    good = np.setdiff1d(np.arange(n), np.union1d(bad_slot, bad_pos))
+    pool_o = np.zeros(slots * bpt, np.uint8)
+    assert O.store(O.FP4, 6, flags, _bf16_np(x)[good], loc.numpy()[good], pool_o, cos_sin=cs.numpy(),
+                   pos=pos.numpy()[good]) == O.OK
+    assert (np_u8(pool) == pool_o).all()
