@@ -2,21 +2,28 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
-A step is one pass of the write path over one batch of synthetic input.  The
-default workload is the fused K RMSNorm + RoPE + V41 store of 16384 bf16 rows
-into a 2^20-slot paged pool (the largest batch of the store sweep); other
-workloads (--workload) cover the plain and RoPE V41 stores, the FP4 store,
-the full-pool and selected-slot dequants, the translated C4A compressor, the
-mixed C128A compressor (both layouts), the decode-time C4A compressor, a
-61-layer step behind one translation (with the per-layer form timed beside
-it), and `sweep`, a hot-L2 latency table at bs 1 / 8 / 64 / 512.
+A step is one pass of the write path over one batch of synthetic input.  With
+no --workload the headline is the mixed C128A compressor (256 requests of
+log-uniform length, about 1.5 M fp32 value + score rows pooled 128 to one
+into a V41 pool: the largest configuration of the path), and every other
+configured workload is timed in the same run and reported under
+"workloads": the small fp32 store + dequant, the store / store + RoPE /
+fused K norm + RoPE V41 stores at 16384 tokens, the FP4 store at 16384 and
+262144 tokens, the FP4 full-pool and selected-slot dequants, the translated
+C4A compressor, C128A into FP4, the decode-time C4A compressor, a 61-layer
+step behind one translation, and the hot-L2 latency table at bs 1/8/64/512.
+--workload NAME times that workload alone (--suite adds the others).
 
-The timed region replays CUDA graphs holding exactly K steps (captured
-launches of the C ABI), bracketed by a barrier and a synchronize, timed with
-CUDA events on the launching stream; inputs rotate over enough distinct sets
-that every step reads from HBM (the rotation set exceeds the 129 MB L2).
-Rank 0 prints one JSON line.  --impl reference times the CPU oracle on a
-bounded sample of the same workload instead.
+Timing, per workload: W eager warm-up steps; CUDA graphs holding exactly K
+steps (captured launches of the C ABI) are replayed between two CUDA events
+on the launching stream, behind a bounded device-side sleep so that the host
+has queued every replay before the first event (the region holds GPU
+execution only, not submission); then the dominant kernel alone is replayed
+in graphs for at least about 25 ms (the per-launch time behind
+roofline.achieved).  Inputs rotate over enough distinct sets that every step
+reads from HBM (each rotation set exceeds the 129 MB L2).  Rank 0 prints one
+JSON line.  --impl reference times the CPU oracle (one thread and one thread
+per host core) on a bounded sample of the same workload instead.
 """
 from __future__ import annotations
 
@@ -50,14 +57,19 @@ def b_compress(r, payload=528):
 
 
 DEFAULT_STEPS = {
-    "store_norm_rope": 200000, "store_rope": 200000, "store": 200000, "small": 200000,
-    "fp4_store": 20000, "fp4_store_16k": 200000, "fp4_dequant": 3000, "c4a": 20000, "c128a": 1000, "c128a_fp4": 1000,
-    "layers": 2000, "dequant_select": 3000, "c4a_decode": 20000,
+    "store_norm_rope": 20, "store_rope": 20, "store": 20, "small": 20,
+    "fp4_store": 20, "fp4_store_16k": 20, "fp4_dequant": 20, "c4a": 20, "c128a": 20, "c128a_fp4": 20,
+    "layers": 20, "dequant_select": 20, "c4a_decode": 20,
 }
+HEADLINE = "c128a"
+# the rest of the configured workloads, timed in the same run as the headline
+SUITE = ["small", "store", "store_rope", "store_norm_rope", "fp4_store_16k", "fp4_store", "fp4_dequant",
+         "dequant_select", "c4a", "c4a_decode", "c128a_fp4", "layers"]
 
 # the workloads: one per configuration of the write path
 SPECS = {
-    "small": dict(kind="store", flags=0, bs=64, pool_slots=256, layout=1, fp32=True),
+    # 64 fp32 rows into a 4-page V41 pool, followed by the dequant of the 4 pages
+    "small": dict(kind="store", flags=0, bs=64, pool_slots=256, layout=1, fp32=True, dequant=True),
     "store": dict(kind="store", flags=0, bs=16384, pool_slots=1 << 20, layout=1),
     "store_rope": dict(kind="store", flags=1, bs=16384, pool_slots=1 << 20, layout=1),
     "store_norm_rope": dict(kind="store", flags=3, bs=16384, pool_slots=1 << 20, layout=1),
@@ -96,6 +108,8 @@ def describe(name):
             cfg["rope"] = "last 64 dims, theta 1e4, positions U[0,65536), fp32 table"
         if sp["flags"] & 2:
             cfg["norm"] = "RMSNorm over 512 dims, w~N(1,0.1), eps 1e-6"
+        if sp.get("dequant"):
+            cfg["dequant"] = "the pool's pages back to bf16 after the store (identity page table)"
         return cfg, "tokens"
     if sp["kind"] == "dequant":
         return {"workload": name, "layout": lay, "tokens": sp["pool_slots"], "page_size": 64,
@@ -191,6 +205,12 @@ class StoreWorkload(Workload):
         per = row_bytes + 8 + payload + ((4 + 256) if self.flags & 1 else 0)
         self.bytes_total = self.bytes_dominant = bs * per
         self.dominant = "store_warp_kernel" if self.layout == 1 else "store_pair_kernel"
+        if sp.get("dequant"):   # the pool's pages back to bf16 after each store
+            self.n_pages = self.pool_slots >> 6
+            self.pt = torch.arange(self.n_pages, dtype=torch.int32, device=dev)
+            self.ws = torch.empty((self.pool_slots, 512), dtype=torch.bfloat16, device=dev)
+            self.launches = 2
+            self.bytes_total += self.pool_slots * (payload + 1024) + self.n_pages * 4
         total = self.R * bs * (row_bytes + 12)
         self.config["l2"] = (f"rotating {self.R} input sets ({total / 2**20:.0f} MB > 129 MB L2)"
                              if total > L2_BYTES else
@@ -203,6 +223,12 @@ class StoreWorkload(Workload):
                          cos_sin=self.cs if rope else None, pos=pos if rope else None, err=self.err)
 
     def step(self, i):
+        r = i % self.R
+        self._store(self.x[r], self.loc[r], self.pos[r])
+        if self.spec.get("dequant"):
+            self.K.kvq_dequant(self.layout, 6, self.pool, self.n_pages, self.pt, self.ws, err=self.err)
+
+    def dominant_step(self, i):
         r = i % self.R
         self._store(self.x[r], self.loc[r], self.pos[r])
 
@@ -251,6 +277,8 @@ class StoreWorkload(Workload):
         compute.wait_event(self.copied[b])
         dx, dloc, dpos = self.dviews[b]
         self._store(dx, dloc, dpos)
+        if self.spec.get("dequant"):
+            self.K.kvq_dequant(self.layout, 6, self.pool, self.n_pages, self.pt, self.ws, err=self.err)
         self.done[b].record(compute)
         self.herr.copy_(self.err, non_blocking=True)
 
@@ -588,11 +616,13 @@ def make_workload(name, dev, tokens=None):
 # ----------------------------------------------------------------------------- clocks
 
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons while running."""
+    """nvidia-smi samples of SM clock, utilisation and throttle reasons while
+    running; samples with the GPU busy count as under load."""
 
-    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+    FIELDS = ("clocks.sm,clocks.max.sm,utilization.gpu,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
+    REASONS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
     def __init__(self, gpu_id):
         self.gpu_id = gpu_id
@@ -623,24 +653,33 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.t.join(timeout=2)
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        return self.summarise(self.lines)
+
+    @classmethod
+    def summarise(cls, lines):
+        busy, idle, mx, reasons = [], [], [], set()
+        for ln in lines:
             parts = [p.strip() for p in ln.split(",")]
-            if len(parts) != 6:
+            if len(parts) != 7:
                 continue
             try:
-                sm.append(float(parts[0]))
-                mx.append(float(parts[1]))
+                sm, smax = float(parts[0]), float(parts[1])
+                util = float(parts[2])
             except ValueError:
                 continue
-            for nm, p in zip(names, parts[2:]):
-                if p.lower() == "active":
-                    reasons.add(nm)
-        if not sm:
+            mx.append(smax)
+            if util >= 50:
+                busy.append(sm)
+                for nm, p in zip(cls.REASONS, parts[3:]):
+                    if p.lower() == "active":
+                        reasons.add(nm)
+            else:
+                idle.append(sm)
+        if not busy and not idle:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
-                "reasons": sorted(reasons)}
+        use = busy or idle
+        return {"sm_mhz": statistics.median(use), "sm_max_mhz": max(mx), "samples": len(use),
+                "samples_total": len(busy) + len(idle), "under_load": bool(busy), "reasons": sorted(reasons)}
 
 
 # ----------------------------------------------------------------------------- helpers
@@ -716,9 +755,38 @@ def dist_env():
     return rank, world, local
 
 
-def capture_graphs(wl, steps, chunk, stream):
-    """CUDA graphs holding exactly `steps` steps: (graph, replays) pairs."""
+def host_cpu():
+    """(model name, usable cores) of this host."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.lower().startswith("model name:"):
+                model = ln.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if not model:
+        try:
+            for ln in open("/proc/cpuinfo"):
+                if ln.lower().startswith(("model name", "cpu part")):
+                    model = ln.split(":", 1)[1].strip()
+                    break
+        except OSError:
+            pass
+    import platform
+    try:
+        cores = len(os.sched_getaffinity(0))
+    except AttributeError:
+        cores = os.cpu_count() or 1
+    return f"{model or 'unknown'} ({platform.machine()})", cores
+
+
+def capture_graphs(wl, steps, chunk, stream, fn=None):
+    """CUDA graphs holding exactly `steps` calls of fn (default: wl.step):
+    (graph, replays) pairs."""
     import torch
+    fn = fn or wl.step
     plan = []
     full, rem = divmod(steps, chunk)
     offset = 0
@@ -728,19 +796,108 @@ def capture_graphs(wl, steps, chunk, stream):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
             for i in range(n):
-                wl.step(offset + i)
+                fn(offset + i)
         plan.append((g, reps))
         offset += n
     return plan
 
 
-def capture_dominant(wl, n, stream):
+# A device-side sleep ahead of each timed region, long enough for the host to
+# queue every graph replay of the region before the GPU reaches the first
+# event: the region then holds GPU execution only.
+SLEEP_CYCLES = 20_000_000  # about 10 ms at the 2.07 GHz SM clock
+
+
+def time_plan(plan, stream):
+    """Milliseconds between two events around the replays of `plan`, queued
+    behind a bounded device-side sleep."""
     import torch
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g, stream=stream):
-        for i in range(n):
-            wl.dominant_step(i)
-    return g
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(SLEEP_CYCLES)
+        e0.record(stream)
+        for g, reps in plan:
+            for _ in range(reps):
+                g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1)
+
+
+def replay_once(plan, stream):
+    import torch
+    with torch.cuda.stream(stream):
+        for g, _ in plan:
+            g.replay()
+    torch.cuda.synchronize()
+
+
+def dominant_launch_ms(wl, stream, est_ms, target_ms=25.0, min_launches=50, chunk_max=512):
+    """Per-launch time of the dominant kernel alone, replayed in graphs for at
+    least about target_ms (inputs rotating as in the step)."""
+    n = int(max(min_launches, min(200_000, math.ceil(target_ms / max(est_ms, 1e-4)))))
+    chunk = min(n, chunk_max)
+    n = max(chunk, (n // chunk) * chunk)
+    plan = capture_graphs(wl, n, chunk, stream, fn=wl.dominant_step)
+    replay_once(plan, stream)
+    ms = time_plan(plan, stream)
+    del plan
+    return ms / n, n
+
+
+def run_workload(wl, K, W, stream, dev, world):
+    """The timed K-step region and the dominant kernel's per-launch time."""
+    import torch
+    with torch.cuda.stream(stream):
+        for i in range(W):
+            wl.step(i)
+    stream.synchronize()
+    assert wl.err.item() == 0, f"device error during warm-up of {wl.name}"
+    chunk = max(1, min(K, max(wl.R, 1) * max(1, 512 // max(wl.R, 1))))
+    plan = capture_graphs(wl, K, chunk, stream)
+    replay_once(plan, stream)  # uploads the graphs
+    import torch.distributed as dist
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ms = time_plan(plan, stream)
+    if world > 1:
+        dist.barrier()
+    del plan
+    assert wl.err.item() == 0, f"device error in the timed region of {wl.name}"
+    ms = max_over_ranks(ms, dev)
+    ms_per_step = ms / K
+    dom_ms, dom_n = dominant_launch_ms(wl, stream, ms_per_step / max(1, wl.launches))
+    dom_ms = max_over_ranks(dom_ms, dev)
+    assert wl.err.item() == 0, f"device error in the dominant-kernel replay of {wl.name}"
+    return ms, ms_per_step, dom_ms, dom_n
+
+
+def workload_record(wl, K, ms, ms_per_step, dom_ms, dom_n, world, peak):
+    achieved = wl.bytes_dominant / (dom_ms / 1e3) / 1e9
+    rec = {
+        "value": wl.units * K * world / (ms / 1e3), "unit": f"{wl.unit_name}/s", "ms_per_step": ms_per_step,
+        "step_gbs": wl.bytes_total / (ms_per_step / 1e3) / 1e9,
+        "kernel": wl.dominant, "kernel_us_per_launch": dom_ms * 1e3, "kernel_launches_timed": dom_n,
+        "algorithmic_bytes_per_launch": wl.bytes_dominant, "achieved_gbs": achieved, "frac": achieved / peak,
+        "traffic": traffic_from_profiles(wl.name), "launches_per_step": wl.launches,
+    }
+    if wl.launches == 1:
+        # the K-step region and the long replay time the same launches
+        rec["k_steps_vs_long_replay"] = ms_per_step / dom_ms
+    return rec
+
+
+def hoist_record(wl, K, ms_per_step, stream):
+    """The layers step with the slot translation repeated inside every layer
+    (the un-hoisted form), timed the same way."""
+    n = max(K, 50)
+    plan = capture_graphs(wl, n, min(n, 64), stream, fn=wl.step_unhoisted)
+    replay_once(plan, stream)
+    un_ms = time_plan(plan, stream) / n
+    return {"hoisted_ms_per_step": ms_per_step, "translate_per_layer_ms_per_step": un_ms,
+            "speedup": un_ms / ms_per_step, "layers": wl.L}
 
 
 # ----------------------------------------------------------------------------- arms
@@ -761,97 +918,21 @@ def run_ours(args):
     import __graft_entry__
     __graft_entry__.build()
 
-    wl = make_workload(args.workload, dev, args.tokens)
-    K = args.steps
-    W = args.warmup
+    K, W = args.steps, args.warmup
     stream = torch.cuda.Stream(device=dev)
-
-    # warm-up: W eager steps through the API
-    with torch.cuda.stream(stream):
-        for i in range(W):
-            wl.step(i)
-    stream.synchronize()
-    assert wl.err.item() == 0, "device error during warm-up"
-
-    chunk = min(K, max(wl.R, 1) * max(1, 512 // max(wl.R, 1)))
-    chunk = max(1, chunk)
-    plan = capture_graphs(wl, K, chunk, stream)
-    # one untimed replay uploads the graphs
-    with torch.cuda.stream(stream):
-        for g, _ in plan:
-            g.replay()
-    torch.cuda.synchronize()
-
+    peak, peak_src = measured_hbm_peak()
     vis = os.environ.get("CUDA_VISIBLE_DEVICES")
     sampler = ClockSampler(vis.split(",")[local] if vis else local)
     if rank == 0 and not args.no_clocks:
         sampler.start()
         time.sleep(0.3)
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    with torch.cuda.stream(stream):
-        for g, reps in plan:
-            for _ in range(reps):
-                g.replay()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
-    clocks = sampler.stop() if (rank == 0 and not args.no_clocks) else None
-    ms = e0.elapsed_time(e1)
-    assert wl.err.item() == 0, "device error in the timed region"
-    ms = max_over_ranks(ms, dev)
-    ms_per_step = ms / K
-    units_all = wl.units * K * world
-    value = units_all / (ms / 1e3)
 
-    # dominant kernel alone (for multi-kernel steps), same launch shape
-    if wl.launches > 1:
-        nd = min(K, chunk)
-        gd = capture_dominant(wl, nd, stream)
-        with torch.cuda.stream(stream):
-            gd.replay()
-        torch.cuda.synchronize()
-        d0 = torch.cuda.Event(enable_timing=True)
-        d1 = torch.cuda.Event(enable_timing=True)
-        d0.record(stream)
-        with torch.cuda.stream(stream):
-            gd.replay()
-        d1.record(stream)
-        torch.cuda.synchronize()
-        dom_ms = d0.elapsed_time(d1) / nd
-    else:
-        dom_ms = ms_per_step
-    # the same step with the slot translation inside every layer (the un-hoisted form)
-    hoist = None
-    if hasattr(wl, "step_unhoisted"):
-        nu = min(K, chunk)
-        gu = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(gu, stream=stream):
-            for i in range(nu):
-                wl.step_unhoisted(i)
-        with torch.cuda.stream(stream):
-            gu.replay()
-        torch.cuda.synchronize()
-        u0 = torch.cuda.Event(enable_timing=True)
-        u1 = torch.cuda.Event(enable_timing=True)
-        u0.record(stream)
-        with torch.cuda.stream(stream):
-            gu.replay()
-        u1.record(stream)
-        torch.cuda.synchronize()
-        un_ms = u0.elapsed_time(u1) / nu
-        hoist = {"hoisted_ms_per_step": ms_per_step, "translate_per_layer_ms_per_step": un_ms,
-                 "speedup": un_ms / ms_per_step, "layers": wl.L}
-    peak, peak_src = measured_hbm_peak()
-    achieved = wl.bytes_dominant / (dom_ms / 1e3) / 1e9
-    step_gbs = wl.bytes_total / (ms_per_step / 1e3) / 1e9
+    wl = make_workload(args.workload, dev, args.tokens)
+    ms, ms_per_step, dom_ms, dom_n = run_workload(wl, K, W, stream, dev, world)
+    head = workload_record(wl, K, ms, ms_per_step, dom_ms, dom_n, world, peak)
+    hoist = hoist_record(wl, K, ms_per_step, stream) if hasattr(wl, "step_unhoisted") else None
 
-    # end to end through the API: pinned host inputs -> device, result word back
+    # end to end through the API: pinned host inputs -> device, result back, every step
     h2d, d2h = wl.e2e_setup()
     e2e_steps = max(3, min(K, args.e2e_steps))
     with torch.cuda.stream(stream):
@@ -865,30 +946,54 @@ def run_ours(args):
         for _ in range(e2e_steps):
             wl.e2e_step()
     stream.synchronize()
-    e2e_s = time.perf_counter() - t0
-    e2e_s = max_over_ranks(e2e_s, dev)
+    e2e_s = max_over_ranks(time.perf_counter() - t0, dev)
     e2e_value = wl.units * e2e_steps * world / e2e_s
+    config = dict(wl.config, units=wl.unit_name, parallelism=f"replicas{world}",
+                  timing="CUDA graphs of exactly K steps behind a device-side sleep (GPU execution only), "
+                         "CUDA events; per-launch kernel time from a >= 25 ms replay of the dominant kernel")
+    launches = wl.launches * K
+    name = wl.name
+    del wl
+    torch.cuda.empty_cache()
+
+    # every other configured workload, timed in the same run
+    suite = {}
+    names = [n for n in SUITE if n != name] if args.suite else []
+    for n in names:
+        w2 = make_workload(n, dev)
+        r = run_workload(w2, K, W, stream, dev, world)
+        suite[n] = workload_record(w2, K, *r, world, peak)
+        if hasattr(w2, "step_unhoisted"):
+            suite[n]["hoist"] = hoist_record(w2, K, r[1], stream)
+        suite[n]["config"] = w2.config
+        del w2
+        torch.cuda.empty_cache()
+    latency = run_latency_table(dev, stream) if (args.suite and rank == 0) else None
+    clocks = sampler.stop() if (rank == 0 and not args.no_clocks) else None
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(wl.name, args.cpu_seconds)
+        cpu = cpu_baseline(name, args.cpu_seconds)
 
     if rank == 0:
         line = {
-            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
+            "metric": METRIC, "value": head["value"], "unit": "tokens/s", "n_gpus": world, "steps": K,
             "warmup": W, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": dict(wl.config, units=wl.unit_name, parallelism=f"replicas{world}",
-                           timing="CUDA graphs of the K steps, CUDA events, 1 untimed upload replay"),
-            "gbs": step_gbs,
-            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "peak_source": f"{peak_src} hbm_gbs (of {peak_src})",
-                         "kernel": wl.dominant, "algorithmic_bytes": wl.bytes_dominant,
-                         "traffic": traffic_from_profiles(wl.name)},
+            "config": config,
+            "gbs": head["step_gbs"],
+            "roofline": {"bound": "hbm", "achieved": head["achieved_gbs"], "peak": peak, "unit": "GB/s",
+                         "frac": head["frac"], "peak_source": f"{peak_src} hbm_gbs (of {peak_src})",
+                         "kernel": head["kernel"], "algorithmic_bytes": head["algorithmic_bytes_per_launch"],
+                         "kernel_us_per_launch": head["kernel_us_per_launch"],
+                         "kernel_launches_timed": head["kernel_launches_timed"],
+                         "traffic": head["traffic"]},
             "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": e2e_steps},
-            "gpu_launches": wl.launches * K,
+            "gpu_launches": launches,
             **({"hoist": hoist} if hoist else {}),
+            **({"workloads": suite} if suite else {}),
+            **({"latency_us": latency} if latency else {}),
             "clocks": clocks,
             "cpu_baseline": cpu,
         }
@@ -934,38 +1039,46 @@ def oracle_sample(name, n_rows):
                 cs=synth.rope_table(65536, "cpu").numpy())
 
 
-def oracle_run(name, smp, n_units):
-    """Run the oracle over about n_units tokens of the sample; returns the tokens done."""
+def oracle_run(name, smp, n_units, first=0):
+    """Run the oracle over about n_units tokens of the sample, starting at unit
+    `first` (wrapping); returns the tokens done."""
     import numpy as np
     import oracle as O
     spec = SPECS[name]
     kind = spec["kind"]
     layout = spec.get("layout", 1)
     if kind == "select":
-        n = max(1, min(n_units, smp["slots"].size))
-        rc, _ = O.dequant_slots(O.FP4, smp["pool"], smp["slots"][:n], 6)
+        size = smp["slots"].size
+        n = max(1, min(n_units, size))
+        a = first % max(1, size - n + 1)
+        rc, _ = O.dequant_slots(O.FP4, smp["pool"], smp["slots"][a:a + n], 6)
         assert rc == O.OK
         return n
     if kind in ("store", "layers"):
-        n = min(n_units, smp["x"].shape[0])
+        size = smp["x"].shape[0]
+        n = min(n_units, size)
+        a = first % max(1, size - n + 1)
         slots = max(64, -(-n // 64) * 64)
         pool = np.zeros(slots * O.bytes_per_token(layout), np.uint8)
-        rc = O.store(layout, 6, spec["flags"], smp["x"][:n], np.arange(n), pool, norm_weight=smp["w"],
-                     eps=1e-6, cos_sin=smp["cs"], pos=smp["pos"][:n])
+        rc = O.store(layout, 6, spec["flags"], smp["x"][a:a + n], np.arange(n), pool, norm_weight=smp["w"],
+                     eps=1e-6, cos_sin=smp["cs"], pos=smp["pos"][a:a + n])
         assert rc == O.OK
         return n
     if kind == "dequant":
-        n_pages = max(1, min(n_units // 64, smp["pages"].size // (64 * 288)))
-        rc, _ = O.dequant(O.FP4, 6, smp["pages"][: n_pages * 64 * 288],
-                          np.arange(n_pages, dtype=np.int32), n_pages * 64)
+        pages = smp["pages"].size // (64 * 288)
+        n_pages = max(1, min(n_units // 64, pages))
+        a = (first // 64) % max(1, pages - n_pages + 1)
+        rc, _ = O.dequant(O.FP4, 6, smp["pages"], np.arange(a, a + n_pages, dtype=np.int32), n_pages * 64)
         assert rc == O.OK
         return n_pages * 64
     r = spec["ratio"]
-    g = max(1, min(n_units // r, smp["gpos"].size))
+    size = smp["gpos"].size
+    g = max(1, min(n_units // r, size))
+    a = (first // r) % max(1, size - g + 1)
     slots = max(64, -(-g // 64) * 64)
     pool = np.zeros(slots * O.bytes_per_token(layout), np.uint8)
-    rc = O.compress(layout, 6, r, O.ROPE, smp["v"][: g * r], smp["s"][: g * r], np.arange(g), pool,
-                    cos_sin=smp["cs"], group_pos=smp["gpos"][:g])
+    rc = O.compress(layout, 6, r, O.ROPE, smp["v"][a * r:(a + g) * r], smp["s"][a * r:(a + g) * r], np.arange(g),
+                    pool, cos_sin=smp["cs"], group_pos=smp["gpos"][a:a + g])
     assert rc == O.OK
     return g * r
 
@@ -973,7 +1086,7 @@ def oracle_run(name, smp, n_units):
 def _sample_rows(name):
     spec = SPECS[name]
     if spec["kind"] in ("compress", "decode"):
-        return spec["ratio"] * (16 if spec["ratio"] >= 128 else 1024)
+        return spec["ratio"] * (64 if spec["ratio"] >= 128 else 1024)
     return min(4096, spec.get("bs", 4096))
 
 
@@ -984,23 +1097,51 @@ def _chunk_units(name):
     return min(256, spec.get("bs", 256))
 
 
-def cpu_baseline(name, seconds):
-    """The oracle (single-threaded C) on a bounded sample of the workload."""
-    smp = oracle_sample(name, _sample_rows(name))
+def oracle_timed(name, smp, seconds, threads):
+    """The oracle over disjoint chunks of the sample for about `seconds`, on
+    `threads` host threads (the C oracle releases the GIL while it runs).
+    Returns (units done, seconds)."""
+    import concurrent.futures as cf
     chunk = _chunk_units(name)
-    done = 0
+    stop = time.perf_counter() + seconds
+
+    def worker(k):
+        done, i = 0, 0
+        while time.perf_counter() < stop:
+            done += oracle_run(name, smp, chunk, first=(k + i * threads) * chunk)
+            i += 1
+        return done
+
     t0 = time.perf_counter()
-    while time.perf_counter() - t0 < seconds:
-        done += oracle_run(name, smp, chunk)
-    dt = time.perf_counter() - t0
-    return {"value": done / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-            "sample": f"{done} {describe(name)[1]} of the {name} workload in {dt:.1f} s "
-                      f"(chunks of {chunk}), single-threaded C oracle, gcc -O2"}
+    if threads == 1:
+        done = worker(0)
+    else:
+        with cf.ThreadPoolExecutor(max_workers=threads) as ex:
+            done = sum(ex.map(worker, range(threads)))
+    return done, time.perf_counter() - t0
+
+
+def cpu_baseline(name, seconds):
+    """The oracle (plain C, built -O2 without FMA contraction) on a bounded
+    sample of the workload: one host thread, then one thread per host core
+    over disjoint chunks; value = the all-core figure."""
+    import oracle as O
+    O.build()
+    smp = oracle_sample(name, _sample_rows(name))
+    model, cores = host_cpu()
+    units = describe(name)[1]
+    d1, t1 = oracle_timed(name, smp, seconds / 2, 1)
+    dn, tn = oracle_timed(name, smp, seconds / 2, cores)
+    return {"value": dn / tn, "unit": "tokens/s", "cores": cores, "kind": "oracle", "cpu": model,
+            "single_thread": {"value": d1 / t1, "unit": "tokens/s", "cores": 1},
+            "sample": f"{dn} {units} of the {name} workload in {tn:.1f} s on {cores} threads (disjoint chunks "
+                      f"of {_chunk_units(name)}); one thread: {d1} in {t1:.1f} s; C oracle, gcc -O2"}
 
 
 def run_reference(args):
-    """The CPU oracle as the reference arm, on the same workload and metric.
-    Runs no GPU code; under torchrun only rank 0 works."""
+    """The CPU oracle as the reference arm, on the same workload and metric,
+    one thread per host core over disjoint chunks.  Runs no GPU code; under
+    torchrun only rank 0 works."""
     rank, world, _ = dist_env()
     if rank != 0:
         return
@@ -1008,21 +1149,16 @@ def run_reference(args):
     O.build()
     name = args.workload
     smp = oracle_sample(name, _sample_rows(name))
+    model, cores = host_cpu()
     K, W = args.steps, args.warmup
-    chunk = _chunk_units(name)
-    t0 = time.perf_counter()
-    u0 = oracle_run(name, smp, chunk)
-    per_unit = (time.perf_counter() - t0) / u0
-    per_step = int(args.ref_seconds / max(1, K + W) / per_unit)
-    per_step = max(chunk if SPECS[name]["kind"] in ("compress", "decode") else 1,
-                   min(per_step, _sample_rows(name)))
+    per_step_s = args.ref_seconds / max(1, K + W)
     for _ in range(W):
-        oracle_run(name, smp, per_step)
-    done = 0
-    t0 = time.perf_counter()
+        oracle_timed(name, smp, per_step_s, cores)
+    done, dt = 0, 0.0
     for _ in range(K):
-        done += oracle_run(name, smp, per_step)
-    dt = time.perf_counter() - t0
+        d, t = oracle_timed(name, smp, per_step_s, cores)
+        done += d
+        dt += t
     value = done / dt
     config, unit_name = describe(name)
     line = {
@@ -1030,35 +1166,27 @@ def run_reference(args):
         "steps": K, "warmup": W, "ms_per_step": dt * 1e3 / K, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": dict(config, units=unit_name, parallelism="cpu oracle, rank 0 only"),
-        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                         "sample": f"{done // K} {unit_name} per step of the {name} workload"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle", "cpu": model,
+                         "sample": f"{done // K} {unit_name} per step of the {name} workload on {cores} "
+                                   f"threads (disjoint chunks of {_chunk_units(name)})"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
 
 
-def run_sweep(args):
+def run_latency_table(dev, stream, reps=1000):
     """Per-launch latency of the store family and the c1 / c2 decode compressors
     at the small batches of the store-latency table ([P1], bs 1/8/64/512):
     CUDA graphs of back-to-back launches on one set of inputs (hot L2, as a
     latency microbenchmark), per-launch time = graph time / launches, the best
     of five replays."""
     import torch
-    rank, world, local = dist_env()
-    if rank != 0:
-        return
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    import __graft_entry__
-    __graft_entry__.build()
     import compress_kv_write_gb300 as K
     from compress_kv_write_gb300 import synth
     pool_slots = 1 << 20
     pool = torch.zeros(pool_slots * 528, dtype=torch.uint8, device=dev)
     cs = synth.rope_table(65536, dev)
     w = synth.norm_weight(dev, 0)
-    stream = torch.cuda.Stream(device=dev)
-    reps = max(1000, args.steps)
 
     def timed(fn):
         with torch.cuda.stream(stream):
@@ -1069,19 +1197,9 @@ def run_sweep(args):
         with torch.cuda.graph(g, stream=stream):
             for _ in range(reps):
                 fn()
-        with torch.cuda.stream(stream):
-            g.replay()
-        torch.cuda.synchronize()
-        best = float("inf")
-        for _ in range(5):  # the best of five replays (short regions are sensitive to clock ramps)
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            with torch.cuda.stream(stream):
-                g.replay()
-            e1.record(stream)
-            torch.cuda.synchronize()
-            best = min(best, e0.elapsed_time(e1) * 1e3 / reps)
-        return best
+        replay_once([(g, 1)], stream)
+        best = min(time_plan([(g, 1)], stream) for _ in range(5))  # short regions: best of five
+        return best * 1e3 / reps
 
     table = {}
     for bs in (1, 8, 64, 512):
@@ -1100,13 +1218,31 @@ def run_sweep(args):
             us = timed(lambda: K.kvq_compress_decode(1, 6, r, K.FLAG_ROPE, v, sc, state, count, loc32, pool,
                                                      pool_slots, cos_sin=cs, group_pos=pos))
             table.setdefault(name, {})[bs] = round(us, 3)
+    del pool
+    torch.cuda.empty_cache()
+    return table
+
+
+def run_sweep(args):
+    """The latency table alone, as its own JSON line."""
+    import torch
+    rank, world, local = dist_env()
+    if rank != 0:
+        return
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import __graft_entry__
+    __graft_entry__.build()
+    stream = torch.cuda.Stream(device=dev)
+    reps = max(1000, args.steps)
+    table = run_latency_table(dev, stream, reps)
     us512 = table["fused K norm + RoPE"][512]
     line = {
         "metric": METRIC, "value": 512 / (us512 * 1e-6), "unit": "tokens/s", "n_gpus": 1, "steps": reps,
         "warmup": 3, "ms_per_step": us512 / 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": "latency sweep (value: fused K norm + RoPE, V41, bs 512)",
-                   "layout": "V41", "x_dtype": "bf16", "pool_slots": pool_slots,
+                   "layout": "V41", "x_dtype": "bf16", "pool_slots": 1 << 20,
                    "l2": "hot: one input set per batch size (latency microbenchmark)",
                    "c1_c2": "kvq_compress_decode, ratio 1 / 2, one row per request, RoPE"},
         "latency_us": table,
@@ -1119,20 +1255,25 @@ def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=None)
-    ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--workload", default="store_norm_rope",
-                    choices=sorted(DEFAULT_STEPS) + ["sweep"])
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=None, choices=sorted(DEFAULT_STEPS) + ["sweep"],
+                    help=f"time one workload (default: {HEADLINE} as the headline, with every other "
+                         "configured workload timed in the same run)")
+    ap.add_argument("--suite", action="store_true", help="with --workload: time the other workloads too")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--e2e-steps", type=int, default=200)
-    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-seconds", type=float, default=20.0)
     ap.add_argument("--ref-seconds", type=float, default=60.0)
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--tokens", type=int, default=None,
                     help="profiling only: shrink the workload to about this many tokens")
     args = ap.parse_args(argv)
+    if args.workload is None:
+        args.workload = HEADLINE
+        args.suite = args.tokens is None
     if args.steps is None:
-        args.steps = DEFAULT_STEPS.get(args.workload, 1000)
+        args.steps = DEFAULT_STEPS.get(args.workload, 20)
     if args.warmup < 3:
         raise SystemExit("--warmup must be at least 3")
     if args.workload == "sweep":

@@ -143,7 +143,7 @@ __global__ void __launch_bounds__(kDecWarps * 32) compress_decode_kernel(const D
     for (int k = 0; k < K; ++k)
 #pragma unroll
         for (int e = 0; e < 4; ++e)
-            y[k][e] = R == 1 ? (&acc[k].x)[e] : __fdividef((&acc[k].x)[e], (&l[k].x)[e]);  // ratio 1: l = 1
+            y[k][e] = R == 1 ? (&acc[k].x)[e] : __fdiv_rn((&acc[k].x)[e], (&l[k].x)[e]);  // ratio 1: l = 1
     if (kRope && pos_ok && rope_col >= kRopeStart) {
         const float c2[2] = {cs_c.x, cs_c.y}, s2[2] = {cs_s.x, cs_s.y};
 #pragma unroll

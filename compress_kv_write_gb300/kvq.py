@@ -18,7 +18,7 @@ V41, V41_FP4 = 1, 2
 F32, BF16 = 0, 1
 I32, I64 = 0, 1
 FLAG_ROPE, FLAG_NORM = 1, 2
-DEVERR_SLOT, DEVERR_POS, DEVERR_PAGE, DEVERR_LOC, DEVERR_TIMEOUT, DEVERR_STATE = 1, 2, 4, 8, 16, 32
+DEVERR_SLOT, DEVERR_POS, DEVERR_PAGE, DEVERR_LOC, DEVERR_STATE = 1, 2, 4, 8, 32
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CAPACITY, ERR_LAUNCH = 0, 1, 2, 3, 4
 HEAD_DIM = 512
 

@@ -70,8 +70,7 @@ enum {
     KVQ_DEVERR_POS = 2,   /* a RoPE position outside [0, cos_sin_rows) (skipped) */
     KVQ_DEVERR_PAGE = 4,  /* a page-table entry outside [0, pool_pages) (skipped)*/
     KVQ_DEVERR_LOC = 8,   /* a full slot outside the translation table (-> -1)   */
-    KVQ_DEVERR_TIMEOUT = 16, /* an internal pipeline wait ran past its 2 s limit; */
-                             /* the kernel stopped early (output incomplete)      */
+                          /* (bit 16 is unused: no kernel has a bounded wait)    */
     KVQ_DEVERR_STATE = 32    /* a request index outside [0, n_state) or a count   */
                              /* outside [0, ratio): that request is skipped       */
 };
@@ -155,8 +154,10 @@ kvq_status kvq_compress(kvq_layout layout, int page_bits, int ratio, unsigned fl
  * When request i's row is the group's ratio-th, the pooled row acc / sum is
  * rotated by row group_pos[i] of cos_sin (KVQ_FLAG_ROPE), rounded to bf16,
  * quantised and stored into slot loc[i] exactly as kvq_compress does, and
- * count returns to 0; otherwise only state and count change and loc[i],
- * group_pos[i] are not read.  A bad request index or count sets
+ * count returns to 0; otherwise only state and count change and the values
+ * of loc[i] and group_pos[i] are ignored.  The kernel reads both arrays
+ * before it knows the count (to overlap their latency), so they must hold n
+ * readable entries on every call.  A bad request index or count sets
  * KVQ_DEVERR_STATE and skips that request.  Requests in one call must use
  * distinct state slots.  KVQ_FLAG_NORM is not accepted. */
 kvq_status kvq_compress_decode(kvq_layout layout, int page_bits, int ratio, unsigned flags,

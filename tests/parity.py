@@ -7,11 +7,68 @@ and each dequantised GPU value may be off the oracle's pre-quantisation fp32
 value by at most the oracle's own quantisation error plus one grid step at
 that magnitude times the block scale.
 """
+import concurrent.futures as cf
+import os
+
 import numpy as np
 
 import oracle as O
 
 CODE_BUDGET = 1e-3
+THREADS = max(1, min(32, os.cpu_count() or 1))
+
+
+def oracle_map(fn, items, threads=THREADS):
+    """fn over items on host threads (the C oracle releases the GIL while it
+    runs), results in order."""
+    items = list(items)
+    if threads <= 1 or len(items) <= 1:
+        return [fn(it) for it in items]
+    with cf.ThreadPoolExecutor(max_workers=threads) as ex:
+        return list(ex.map(fn, items))
+
+
+def group_prequant_many(ratio, flags, v, s, cs_rows):
+    """The oracle's pre-quantisation rows of G groups: v, s [G*ratio, 512],
+    cs_rows [G, 64] (or None); returns float32 [G, 512]."""
+    G = v.shape[0] // ratio
+    chunks = [(a, min(G, a + 64)) for a in range(0, G, 64)]
+
+    def run(ab):
+        a, b = ab
+        return np.stack([O.group_prequant(ratio, flags, v[i * ratio:(i + 1) * ratio], s[i * ratio:(i + 1) * ratio],
+                                          None if cs_rows is None else cs_rows[i]) for i in range(a, b)])
+    out = oracle_map(run, chunks)
+    return np.concatenate(out) if out else np.zeros((0, 512), np.float32)
+
+
+def token_prequant_many(flags, x, norm_weight, eps, cs_rows):
+    """The oracle's pre-quantisation rows of n tokens x [n, 512]; cs_rows [n, 64]."""
+    n = x.shape[0]
+    chunks = [(a, min(n, a + 256)) for a in range(0, n, 256)]
+
+    def run(ab):
+        a, b = ab
+        return np.stack([O.token_prequant(flags, x[t], norm_weight, eps, None if cs_rows is None else cs_rows[t])
+                         for t in range(a, b)])
+    out = oracle_map(run, chunks)
+    return np.concatenate(out) if out else np.zeros((0, 512), np.float32)
+
+
+def encode_many(layout, y):
+    """Oracle code and scale rows of pre-quantisation rows y [n, 512]."""
+    enc = O.encode_v41 if layout == O.V41 else O.encode_fp4
+    rows = [enc(y[i]) for i in range(y.shape[0])]
+    return np.stack([r[0] for r in rows]), np.stack([r[1] for r in rows])
+
+
+def _log(ndiff, total):
+    """Append the observed difference count to $KVQ_PARITY_LOG (if set)."""
+    path = os.environ.get("KVQ_PARITY_LOG")
+    if path:
+        name = os.environ.get("PYTEST_CURRENT_TEST", "?").split(" ")[0]
+        with open(path, "a") as f:
+            f.write(f"{name} {ndiff} {total} {ndiff / max(1, total):.3e}\n")
 
 
 def np_u8(t):
@@ -88,6 +145,7 @@ def check_tolerance(layout, g_codes, g_scales, o_codes, o_scales, y_oracle, budg
     diff = gd != od
     ndiff = int(diff.sum())
     total = n * 512
+    _log(ndiff, total)
     assert ndiff <= budget * total, f"{ndiff} of {total} elements differ"
     # one grid step at the larger of the two magnitudes, in units of the scale
     mag = np.maximum(np.abs(gd), np.abs(od)) / S

@@ -28,13 +28,21 @@ def test_workload_description_and_oracle_sample(name):
     assert len(bench.kernel_source_sha(name)) == 16
 
 
-def test_traffic_table_matches_current_sources():
-    """Every workload with a committed capture resolves to a traffic figure
-    (the sources have not changed since), and it is close to the algorithmic
-    bytes it was scaled to."""
-    found = {w: bench.traffic_from_profiles(w) for w in bench.SPECS}
-    for w in ("store_norm_rope", "fp4_store", "fp4_dequant", "c4a", "c128a", "c4a_decode", "dequant_select"):
-        assert found[w] is not None and found[w] > 0, w
+def test_traffic_table_follows_the_sources():
+    """A committed capture resolves to its traffic figure only while the
+    dominant kernel's sources are unchanged since it was taken; a stale
+    capture gives None (the JSON line then carries null)."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    rows = [ln.split() for ln in open(path).read().splitlines() if ln.strip() and not ln.startswith("#")]
+    assert rows
+    for p in rows:
+        name, sha = p[0], p[3]
+        assert name in bench.SPECS
+        got = bench.traffic_from_profiles(name)
+        if sha == bench.kernel_source_sha(name):
+            assert got is not None and got > 0, name
+        elif not any(q[0] == name and q[3] == bench.kernel_source_sha(name) for q in rows):
+            assert got is None, name
 
 
 @pytest.mark.parametrize("name", ["store_norm_rope", "fp4_dequant", "c4a"])
@@ -52,7 +60,34 @@ def test_reference_arm_json(name, monkeypatch):
     assert d["impl"] == "reference" and d["n_gpus"] == 1 and d["steps"] == 3 and d["warmup"] == 3
     assert d["value"] > 0 and d["higher_is_better"] is True and d["config"]["workload"] == name
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
-    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] == 1
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["cpu_baseline"]["cpu"]
+
+
+def test_cpu_baseline_threads_and_model():
+    """The CPU baseline reports one thread and one thread per host core, with
+    the host CPU named."""
+    cb = bench.cpu_baseline("store_norm_rope", 0.4)
+    model, cores = bench.host_cpu()
+    assert cb["cores"] == cores >= 1 and cb["cpu"] == model and model
+    assert cb["value"] > 0 and cb["single_thread"]["value"] > 0 and cb["single_thread"]["cores"] == 1
+
+
+def test_default_is_the_largest_config_with_the_suite():
+    """No --workload: the mixed C128A batch is the headline and the suite holds
+    every other configured workload."""
+    assert bench.HEADLINE == "c128a"
+    assert set(bench.SUITE) | {bench.HEADLINE} == set(bench.SPECS)
+
+
+def test_clock_summary_uses_busy_samples():
+    busy = "2070, 2070, 100, Not Active, Not Active, Not Active, Active"
+    idle = "345, 2070, 0, Not Active, Not Active, Not Active, Not Active"
+    c = bench.ClockSampler.summarise([idle, busy, busy, idle])
+    assert c["sm_mhz"] == 2070 and c["samples"] == 2 and c["under_load"]
+    assert c["reasons"] == ["sw_power_cap"]
+    c = bench.ClockSampler.summarise([idle])
+    assert not c["under_load"] and c["sm_mhz"] == 345
 
 
 def test_warmup_floor():

@@ -16,7 +16,8 @@ import pytest
 import torch
 
 import oracle as O
-from parity import (check_tolerance, decode_rows, gather_rows, gather_rows_torch, np_u8)
+from parity import (check_tolerance, decode_rows, encode_many, gather_rows, gather_rows_torch,
+                    group_prequant_many, np_u8, oracle_map, token_prequant_many)
 
 pytestmark = pytest.mark.gpu
 
@@ -84,9 +85,13 @@ def test_fp32_store_and_dequant_64_tokens(K):
 @pytest.mark.parametrize("loc64", [False, True])
 @pytest.mark.parametrize("flags", [0, 1, 2, 3])
 def test_store_instances_ragged(K, page_bits, layout, dtype, loc64, flags):
+    """Every store instance on ragged batches (1, 37, 301 rows): the plain and
+    RoPE paths bit-exact over the whole pool; the norm paths under the
+    tolerance rule, the three batches pooled into one comparison."""
     from compress_kv_write_gb300 import synth
     slots = 1024
     rng_seed = page_bits * 1000 + layout * 100 + flags * 10 + int(loc64)
+    acc = [[], [], [], [], []]
     for n in (1, 37, 301):
         x = synth.store_rows_bf16(n, "cpu", rng_seed + n)
         if dtype == "f32":
@@ -114,11 +119,13 @@ def test_store_instances_ragged(K, page_bits, layout, dtype, loc64, flags):
         else:
             g = gather_rows(got, layout, page_bits, loc.numpy())
             o = gather_rows(pool_o, layout, page_bits, loc.numpy())
-            y = np.stack([O.token_prequant(flags, x_np[t], w.numpy(), 1e-6, cs.numpy()[pos[t]])
-                          for t in range(n)])
-            check_tolerance(layout, g[0], g[1], o[0], o[1], y)
+            y = token_prequant_many(flags, x_np, w.numpy(), 1e-6, cs.numpy()[pos.numpy()])
+            for a, b in zip(acc, (g[0], g[1], o[0], o[1], y)):
+                a.append(b)
             written = int(g[0].astype(np.int64).sum() + g[1].astype(np.int64).sum())
             assert int(got.astype(np.int64).sum()) == written   # nothing else touched
+    if flags & 2:
+        check_tolerance(layout, *[np.concatenate(a) for a in acc])
 
 
 # --------------------------------------------------------------------------- codecs
@@ -233,29 +240,37 @@ def sweep_inputs():
     return x, loc, pos, cs, w
 
 
-@pytest.mark.parametrize("bs", [1, 8, 64, 512, 16384])
 @pytest.mark.parametrize("flags", [0, 1, 3])
-def test_store_batch_sweep(K, sweep_inputs, bs, flags):
+def test_store_batch_sweep(K, sweep_inputs, flags):
     """bf16 rows with outliers, pool of 2^20 slots: store, store + RoPE and
-    fused K RMSNorm + RoPE at every batch size of the sweep."""
-    x, loc, pos, cs, w = sweep_inputs
-    x, loc, pos = x[:bs], loc[:bs], pos[:bs]
-    pool = torch.zeros(POOL_SLOTS_1 * 528, dtype=torch.uint8, device=DEV)
-    err = _err(K)
-    K.kvq_store(K.V41, 6, flags, x, loc, pool, POOL_SLOTS_1, norm_weight=w, eps=1e-6,
-                cos_sin=cs, pos=pos, err=err)
-    torch.cuda.synchronize()
-    assert err.item() == 0
-    g = gather_rows_torch(pool, O.V41, 6, loc.cpu().numpy())
-    x_np, pos_np, cs_np, w_np = _bf16_np(x), pos.cpu().numpy(), cs.cpu().numpy(), w.cpu().numpy()
-    o = _oracle_store_rows(O.V41, flags, x_np, w_np, 1e-6, cs_np, pos_np)
+    fused K RMSNorm + RoPE at every batch size of the sweep (1, 8, 64, 512,
+    16384), each into a fresh pool.  Plain and RoPE stores are bit-exact;
+    the fused norm path follows the tolerance rule with the five batches
+    pooled into one comparison."""
+    x_all, loc_all, pos_all, cs, w = sweep_inputs
+    cs_np, w_np = cs.cpu().numpy(), w.cpu().numpy()
+    acc = [[], [], [], [], []]
+    for bs in (1, 8, 64, 512, 16384):
+        x, loc, pos = x_all[:bs], loc_all[:bs], pos_all[:bs]
+        pool = torch.zeros(POOL_SLOTS_1 * 528, dtype=torch.uint8, device=DEV)
+        err = _err(K)
+        K.kvq_store(K.V41, 6, flags, x, loc, pool, POOL_SLOTS_1, norm_weight=w, eps=1e-6,
+                    cos_sin=cs, pos=pos, err=err)
+        torch.cuda.synchronize()
+        assert err.item() == 0
+        g = gather_rows_torch(pool, O.V41, 6, loc.cpu().numpy())
+        x_np, pos_np = _bf16_np(x), pos.cpu().numpy()
+        o = _oracle_store_rows(O.V41, flags, x_np, w_np, 1e-6, cs_np, pos_np)
+        if flags & 2:
+            y = token_prequant_many(flags, x_np, w_np, 1e-6, cs_np[pos_np])
+            for a, b in zip(acc, (g[0], g[1], o[0], o[1], y)):
+                a.append(b)
+        else:
+            assert (g[0] == o[0]).all() and (g[1] == o[1]).all(), bs
+        written = int(g[0].astype(np.int64).sum() + g[1].astype(np.int64).sum())
+        assert int(pool.sum(dtype=torch.int64).item()) == written
     if flags & 2:
-        y = np.stack([O.token_prequant(flags, x_np[t], w_np, 1e-6, cs_np[pos_np[t]]) for t in range(bs)])
-        check_tolerance(O.V41, g[0], g[1], o[0], o[1], y)
-    else:
-        assert (g[0] == o[0]).all() and (g[1] == o[1]).all()
-    written = int(g[0].astype(np.int64).sum() + g[1].astype(np.int64).sum())
-    assert int(pool.sum(dtype=torch.int64).item()) == written
+        check_tolerance(O.V41, *[np.concatenate(a) for a in acc])
 
 
 # --------------------------------------------------------------------------- FP4 store + dequant
@@ -286,20 +301,26 @@ def test_fp4_store_and_full_pool_dequant(K, bs):
     assert (g[0] == o[0]).all() and (g[1] == o[1]).all()
     written = int(g[0].astype(np.int64).sum() + g[1].astype(np.int64).sum())
     assert int(pool.sum(dtype=torch.int64).item()) == written
-    # dequant: sampled logical pages, oracle on the gathered physical pages
-    rng = np.random.default_rng(bs)
+    # dequant: every logical page, the oracle on host threads in chunks of pages
+    pool_np = np_u8(pool)
     pt_np = pt.cpu().numpy()
-    lps = rng.choice(n_pages, 96, replace=False)
-    # make sure some sampled pages hold stored rows
-    lps = np.unique(np.concatenate([lps, np.flatnonzero(np.isin(pt_np, loc_np[:32] >> 6))]))
-    pb = 64 * 288
-    page_bytes = torch.stack([pool[int(p) * pb:(int(p) + 1) * pb] for p in pt_np[lps]]).cpu().numpy()
-    rc, ws = O.dequant(O.FP4, 6, page_bytes.reshape(-1), np.arange(lps.size, dtype=np.int32), lps.size * 64)
-    assert rc == O.OK
-    rows = (lps[:, None] * 64 + np.arange(64)[None, :]).reshape(-1)
-    got = _bf16_np(out[torch.as_tensor(rows, device=DEV)])
-    assert (got == ws).all()
-    assert np.count_nonzero(ws) > 0
+    chunk = 1024
+    spans = [(a, min(n_pages, a + chunk)) for a in range(0, n_pages, chunk)]
+
+    def ref(ab):
+        a, b = ab
+        rc, ws = O.dequant(O.FP4, 6, pool_np, pt_np[a:b], (b - a) * 64)
+        assert rc == O.OK
+        return ws
+    nonzero = 0
+    for i in range(0, len(spans), 16):
+        part = spans[i:i + 16]
+        for (a, b), ws in zip(part, oracle_map(ref, part)):
+            got = out[a * 64:b * 64].view(torch.int16)
+            want = torch.from_numpy(ws.view(np.int16)).to(DEV)
+            assert torch.equal(got, want), (a, b)
+            nonzero += int(np.count_nonzero(ws))
+    assert nonzero > 0
 
 
 # --------------------------------------------------------------------------- C4A + translation
@@ -338,8 +359,7 @@ def test_translate_and_c4a(K):
     got = np_u8(pool)
     g = gather_rows(got, O.V41, 6, slots)
     o = gather_rows(pool_o, O.V41, 6, slots)
-    y = np.stack([O.group_prequant(r, O.ROPE, v_np[i * r:(i + 1) * r], s_np[i * r:(i + 1) * r],
-                                   cs_np[i * r]) for i in range(G)])
+    y = group_prequant_many(r, O.ROPE, v_np, s_np, cs_np[np.arange(G) * r])
     check_tolerance(O.V41, g[0], g[1], o[0], o[1], y)
     written = int(g[0].astype(np.int64).sum() + g[1].astype(np.int64).sum())
     assert int(got.astype(np.int64).sum()) == written
@@ -348,10 +368,14 @@ def test_translate_and_c4a(K):
 @pytest.mark.parametrize("layout", [1, 2])
 @pytest.mark.parametrize("r", [1, 2, 4, 128])
 def test_compress_small_exhaustive(K, layout, r):
-    """Every compiled ratio, ragged group counts, whole-pool comparison."""
+    """Every compiled ratio on ragged group counts (1, 3, 45 and 97 groups),
+    each launch compared with the oracle over the whole pool.  r = 1 is the
+    identity (bit-exact); for r > 1 the groups of all four launches are
+    pooled into one comparison under the 0.1% code budget."""
     from compress_kv_write_gb300 import synth
     slots = 512
-    for G in (1, 3, 45):
+    gc, gs_, oc, os_, ys = [], [], [], [], []
+    for G in (1, 3, 45, 97):
         v, s = synth.compressor_rows(G * r, "cpu", G + r, score_std=2.0)
         loc = synth.injective_slots(G, slots, "cpu", G, dtype=torch.int32)
         gpos = synth.positions(G, "cpu", G, max_pos=1024)
@@ -366,18 +390,20 @@ def test_compress_small_exhaustive(K, layout, r):
         torch.cuda.synchronize()
         assert err.item() == 0
         got = np_u8(pool)
-        gs = loc.numpy()
-        g = gather_rows(got, layout, 6, gs)
-        o = gather_rows(pool_o, layout, 6, gs)
-        gp = gpos.numpy()
-        y = np.stack([O.group_prequant(r, O.ROPE, v.numpy()[i * r:(i + 1) * r], s.numpy()[i * r:(i + 1) * r],
-                                       cs.numpy()[gp[i]]) for i in range(G)])
+        g = gather_rows(got, layout, 6, loc.numpy())
+        o = gather_rows(pool_o, layout, 6, loc.numpy())
         if r == 1:   # r = 1 pooling is the identity: bit-exact
             assert (g[0] == o[0]).all() and (g[1] == o[1]).all()
-        else:
-            check_tolerance(layout, g[0], g[1], o[0], o[1], y, budget=2e-3 if G * 512 < 5000 else 1e-3)
+        gc.append(g[0])
+        gs_.append(g[1])
+        oc.append(o[0])
+        os_.append(o[1])
+        ys.append(group_prequant_many(r, O.ROPE, v.numpy(), s.numpy(), cs.numpy()[gpos.numpy()]))
         written = int(g[0].astype(np.int64).sum() + g[1].astype(np.int64).sum())
         assert int(got.astype(np.int64).sum()) == written
+    if r > 1:
+        check_tolerance(layout, np.concatenate(gc), np.concatenate(gs_), np.concatenate(oc),
+                        np.concatenate(os_), np.concatenate(ys))
 
 
 # --------------------------------------------------------------------------- C128A mixed batch
@@ -386,7 +412,8 @@ def test_compress_small_exhaustive(K, layout, r):
 def test_c128a_mixed_batch(K, layout):
     """256 requests, log-uniform lengths in [128, 32768] (multiples of 128),
     values N(0,1), scores N(0,4); 128-row groups at positions 128 * local
-    group index; sampled groups against the oracle."""
+    group index.  Every group is compared with the oracle (pooled on host
+    threads, in chunks of groups copied back from the device)."""
     from compress_kv_write_gb300 import synth
     r = 128
     lens = synth.request_lengths(256, seed=0)
@@ -402,22 +429,21 @@ def test_c128a_mixed_batch(K, layout):
                    group_pos=gpos, err=err)
     torch.cuda.synchronize()
     assert err.item() == 0
-    rng = np.random.default_rng(layout)
-    pick = np.unique(np.concatenate([rng.choice(G, 150, replace=False), [0, G - 1]]))
     loc_np, gpos_np, cs_np = loc.cpu().numpy(), gpos.cpu().numpy(), cs.cpu().numpy()
-    g = gather_rows_torch(pool, layout, 6, loc_np[pick])
-    oc, osc, ys = [], [], []
-    for i in pick:
-        vi = v[i * r:(i + 1) * r].cpu().numpy()
-        si = s[i * r:(i + 1) * r].cpu().numpy()
-        c, sc = O.group_bytes(layout, r, O.ROPE, vi, si, cs_np[gpos_np[i]])
-        oc.append(c)
-        osc.append(sc)
-        ys.append(O.group_prequant(r, O.ROPE, vi, si, cs_np[gpos_np[i]]))
-    check_tolerance(layout, g[0], g[1], np.stack(oc), np.stack(osc), np.stack(ys))
-    # every group was written: its scale row is non-zero
-    gs = gather_rows_torch(pool, layout, 6, loc_np)[1]
-    assert (gs[:, :16].astype(np.int64).sum(1) > 0).all()
+    g = gather_rows_torch(pool, layout, 6, loc_np)
+    ys = []
+    step = 1024
+    for a in range(0, G, step):
+        b = min(G, a + step)
+        vi = v[a * r:b * r].cpu().numpy()
+        si = s[a * r:b * r].cpu().numpy()
+        ys.append(group_prequant_many(r, O.ROPE, vi, si, cs_np[gpos_np[a:b]]))
+    y = np.concatenate(ys)
+    oc, osc = encode_many(layout, y)
+    check_tolerance(layout, g[0], g[1], oc, osc, y)
+    # nothing but the groups' rows was written
+    written = int(g[0].astype(np.int64).sum() + g[1].astype(np.int64).sum())
+    assert int(pool.sum(dtype=torch.int64).item()) == written
 
 
 # --------------------------------------------------------------------------- error paths
@@ -552,13 +578,16 @@ def test_dequant_slots_fp4_pool_2m(K):
     K.kvq_dequant_slots(K.V41_FP4, 6, pool, pool_slots, sel, out, err=err)
     torch.cuda.synchronize()
     assert err.item() == 0
-    rng = np.random.default_rng(0)
-    pick = rng.choice(n, 4096, replace=False)
     sel_np = sel.cpu().numpy()
     pool_np = np_u8(pool)
-    rc, ref = O.dequant_slots(O.FP4, pool_np, sel_np[pick], 6)
-    assert rc == O.OK
-    assert (_bf16_np(out[torch.as_tensor(pick, device=DEV)]) == ref).all()
+    spans = [(a, min(n, a + 8192)) for a in range(0, n, 8192)]
+
+    def ref(ab):
+        rc, r_ = O.dequant_slots(O.FP4, pool_np, sel_np[ab[0]:ab[1]], 6)
+        assert rc == O.OK
+        return r_
+    want = np.concatenate(oracle_map(ref, spans))
+    assert (_bf16_np(out) == want).all()
 
 
 # --------------------------------------------------------------------------- more page sizes
@@ -613,9 +642,11 @@ def test_compress_decode_streams(K, layout, r):
     """Rows arrive one per call to a random subset of request slots, in random
     order (state indexed through req); every group a slot completes is
     compared with the oracle's pooling of that group's r rows.  r = 1 is the
-    identity (bit-exact); the others follow the pooling tolerance."""
+    identity (bit-exact); the others follow the pooling tolerance (0.1% code
+    budget over all completed groups: 16 to 48 request slots, so that every
+    ratio completes dozens of groups)."""
     rng = np.random.default_rng(100 * layout + r)
-    n_state = 24 if r < 128 else 6
+    n_state = 48 if r < 128 else 16
     calls = 3 * r + 2 if r < 128 else 2 * r + 3
     pool_slots = max(1024, -(-calls * n_state // 64) * 64)  # a fresh destination per row
     from compress_kv_write_gb300 import synth
@@ -666,7 +697,7 @@ def test_compress_decode_streams(K, layout, r):
     if r == 1:
         assert (g[0] == oc).all() and (g[1] == osc).all()
     else:
-        check_tolerance(layout, g[0], g[1], oc, osc, np.stack(ys), budget=2e-3)
+        check_tolerance(layout, g[0], g[1], oc, osc, np.stack(ys))
     written = int(g[0].astype(np.int64).sum() + g[1].astype(np.int64).sum())
     assert int(got.astype(np.int64).sum()) == written  # open groups wrote nothing
 
@@ -789,11 +820,8 @@ def test_store_many_tokens_per_warp(K, flags):
     else:
         g = gather_rows(got, O.V41, 6, loc_np)
         o = gather_rows(pool_o, O.V41, 6, loc_np)
-        sel = np.arange(0, n, 61)  # the prequant reference for a sample of the rows
-        y = np.stack([O.token_prequant(flags, x_np[t], w_np, 1e-6, cs_np[pos_np[t]]) for t in sel])
-        check_tolerance(O.V41, g[0][sel], g[1][sel], o[0][sel], o[1][sel], y)
-        diff = (g[0] != o[0]).mean()
-        assert diff < 1e-3, diff  # code bytes that differ anywhere in the batch
+        y = token_prequant_many(flags, x_np, w_np, 1e-6, cs_np[pos_np])
+        check_tolerance(O.V41, g[0], g[1], o[0], o[1], y)
 
 
 # --------------------------------------------------------------------------- hand-worked blocks
@@ -875,12 +903,8 @@ def test_bad_rows_in_a_large_batch(K, flags):
     else:
         g = gather_rows(got, O.V41, 6, loc.numpy()[good])
         o = gather_rows(pool_o, O.V41, 6, loc.numpy()[good])
-        assert (g[0] != o[0]).mean() < 1e-3
-        sel = good[::37]
-        gs = gather_rows(got, O.V41, 6, loc.numpy()[sel])
-        os_ = gather_rows(pool_o, O.V41, 6, loc.numpy()[sel])
-        y = np.stack([O.token_prequant(flags, x_np[t], w.numpy(), 1e-6, cs.numpy()[pos[t]]) for t in sel])
-        check_tolerance(O.V41, gs[0], gs[1], os_[0], os_[1], y)
+        y = token_prequant_many(flags, x_np[good], w.numpy(), 1e-6, cs.numpy()[pos.numpy()[good]])
+        check_tolerance(O.V41, g[0], g[1], o[0], o[1], y)
         # nothing outside the good rows' slots was written
         mask = np.zeros(slots, bool)
         mask[loc.numpy()[good]] = True
