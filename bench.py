@@ -889,6 +889,24 @@ def workload_record(wl, K, ms, ms_per_step, dom_ms, dom_n, world, peak):
     return rec
 
 
+def add_l2_flush(wl, dev, nbytes=512 << 20):
+    """Profiling only: read a buffer four times the L2 after every step, so
+    that the lines a step left dirty in L2 are written back to DRAM inside
+    the next kernel (a capture of both kernels then counts the write-back
+    that a capture of the step's kernels alone cannot see)."""
+    import torch
+    buf = torch.ones(nbytes // 4, dtype=torch.float32, device=dev)
+    step, dominant = wl.step, wl.dominant_step
+
+    def flushed(fn):
+        def run(i):
+            fn(i)
+            buf.sum()
+        return run
+    wl.step, wl.dominant_step = flushed(step), flushed(dominant)
+    wl.config["l2_flush"] = f"profiling: a {nbytes >> 20} MB read after every step (not a bench number)"
+
+
 def hoist_record(wl, K, ms_per_step, stream):
     """The layers step with the slot translation repeated inside every layer
     (the un-hoisted form), timed the same way."""
@@ -928,6 +946,8 @@ def run_ours(args):
         time.sleep(0.3)
 
     wl = make_workload(args.workload, dev, args.tokens)
+    if args.flush_l2:
+        add_l2_flush(wl, dev)
     ms, ms_per_step, dom_ms, dom_n = run_workload(wl, K, W, stream, dev, world)
     head = workload_record(wl, K, ms, ms_per_step, dom_ms, dom_n, world, peak)
     hoist = hoist_record(wl, K, ms_per_step, stream) if hasattr(wl, "step_unhoisted") else None
@@ -1268,10 +1288,12 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--tokens", type=int, default=None,
                     help="profiling only: shrink the workload to about this many tokens")
+    ap.add_argument("--flush-l2", action="store_true",
+                    help="profiling only: evict L2 after every step (counts the write-back in ncu)")
     args = ap.parse_args(argv)
     if args.workload is None:
         args.workload = HEADLINE
-        args.suite = args.tokens is None
+        args.suite = args.tokens is None and not args.flush_l2
     if args.steps is None:
         args.steps = DEFAULT_STEPS.get(args.workload, 20)
     if args.warmup < 3:

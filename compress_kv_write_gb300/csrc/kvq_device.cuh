@@ -91,6 +91,13 @@ __device__ __forceinline__ void st_u4(void *p, uint4 v) {
                  : "memory");
 }
 
+// One 32-byte store per lane (p 32-byte aligned).
+__device__ __forceinline__ void st_v8(void *p, const uint32_t (&w)[8]) {
+    asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(w[0]), "r"(w[1]),
+                 "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                 : "memory");
+}
+
 // ---------------------------------------------------------------- conversions
 // Two fp32 -> packed e4m3x2, round to nearest even, saturating to +-448.
 // The first operand of cvt goes to the upper byte.
@@ -168,6 +175,13 @@ __device__ __forceinline__ float ue8m0_to_f32(uint32_t byte) {
     return __uint_as_float(byte << 23);
 }
 
+// max(a, b, c) in one instruction (three-operand fp32 max).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
 // |x| bits, so that an unsigned max is the magnitude max (finite inputs).
 __device__ __forceinline__ uint32_t abs_bits(float x) { return __float_as_uint(x) & 0x7FFFFFFFu; }
 
@@ -197,6 +211,18 @@ __device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
         "mov.b64 pa, {%2, %3};\n\t"
         "mov.b64 pb, {%4, %5};\n\t"
         "mul.rn.f32x2 pr, pa, pb;\n\t"
+        "mov.b64 {%0, %1}, pr;\n\t}"
+        : "=f"(r.x), "=f"(r.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return r;
+}
+
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+    float2 r;
+    asm("{\n\t.reg .b64 pa, pb, pr;\n\t"
+        "mov.b64 pa, {%2, %3};\n\t"
+        "mov.b64 pb, {%4, %5};\n\t"
+        "add.rn.f32x2 pr, pa, pb;\n\t"
         "mov.b64 {%0, %1}, pr;\n\t}"
         : "=f"(r.x), "=f"(r.y)
         : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
@@ -257,6 +283,12 @@ __device__ __forceinline__ void prefetch_l2(const void *p) {
 // Into this SM's L1 as well; issue it only after griddepcontrol.wait.
 __device__ __forceinline__ void prefetch_l1(const void *p) {
     asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
+}
+
+__device__ __forceinline__ uint2 lds_u2(const void *p) {
+    uint2 r;
+    asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "r"(smem_addr(p)));
+    return r;
 }
 
 __device__ __forceinline__ uint4 lds_u4(const void *p) {

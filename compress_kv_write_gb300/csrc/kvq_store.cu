@@ -1,38 +1,40 @@
 // kvq_store.cu -- fused (K RMSNorm) + (RoPE) + block quantisation + paged
 // scatter of new K rows: the store / store + RoPE / fused K norm + RoPE
 // kernels of "[sglang] DeepSeek V4.1 Paged KV Cache: V41 and FP4 formats"
-// (section 1 store_row, and the store-latency table).
+// (section 1 store_row, and the store-latency table), for both layouts.
 //
-// Both kernels are persistent (as many CTAs of four warps as are resident at
-// once; the fused norm + RoPE V41 instance switches to one-warp CTAs from
-// three tokens per resident warp up); warp w of W owns the contiguous token
-// range [n*w/W, n*(w+1)/W) and
-// keeps its next rows in flight in a per-warp shared-memory ring filled with
-// cp.async (one commit group per ring slot; the V41 kernel with RoPE commits
-// a token's cos/sin values as a second group, so that everything but the
-// rotated chunk is finished while they land).  Before the PDL wait each warp
-// prefetches its first rows into L2.  Slot indices and positions of
-// 32 tokens sit one per lane, validated once, and are fetched with a
-// shuffle.  Math is fp32; the products of the RMSNorm and of the rotation are
-// rounded one by one, as in the definition.
+// Two kernels share the structure below and differ in how a token maps onto
+// lanes (launch_store says which instance uses which, and why):
 //
-//  * store_warp_kernel (V41): one warp per token.  Lane l owns the 16-byte
-//    chunks l, l+32, ... of the row, so every warp load / store instruction
-//    covers one contiguous span; a 32-value quant block is 32/(values per
-//    chunk) adjacent lanes, reduced with xor shuffles.  Each lane copies and
-//    reads back only its own chunks: no cross-lane waits.
-//  * store_pair_kernel (V41_FP4): two tokens per warp; half-warp h holds
-//    token 2k+h and lane i of the half owns quant block i.  The block
-//    absmax needs no shuffle and each block's e4m3 scale and reciprocal are
-//    computed once.  Rows land block-swizzled in shared memory so the
-//    block-per-lane reads are bank-conflict-free.
+//  * store_warp_kernel: one warp per token.  Lane l owns the 16-byte chunks
+//    l, l+32, ... of the row, so every warp load / store instruction covers
+//    one contiguous span; a 32-value quant block is 32/(values per chunk)
+//    adjacent lanes, reduced with xor shuffles.  Each lane copies and reads
+//    back only its own chunks: no cross-lane waits.  With RoPE a token's
+//    cos/sin values are a second commit group, so that everything but the
+//    rotated chunk is finished while they land.
+//  * store_half_kernel: two tokens per warp; half-warp h holds token 2k+h
+//    and lane i of the half owns quant block i, so a block's absmax needs no
+//    shuffle and its scale (V41 exponent byte, or FP4 e4m3 scale with its
+//    correctly rounded division and reciprocal) is computed once.  With
+//    RoPE the 64 rotated dims (the last two blocks) are spread over all 16
+//    lanes instead: lane i rotates the quad of dims 448+4i .. 448+4i+3, the
+//    two rotated blocks' absmax is an 8-lane shuffle reduction, and lanes 14
+//    and 15 own no whole block.  Rows land block-swizzled in shared memory
+//    so that the block-per-lane reads are bank-conflict-free; a V41 block's
+//    32 code bytes leave in one 32-byte store per lane.
+//
+// Shared structure: persistent CTAs (as many as are resident at once); warp
+// w owns a contiguous token range computed on the host (partition) and keeps
+// its next rows in flight in a per-warp shared-memory ring filled with
+// cp.async.  Before the PDL wait each warp prefetches its first rows into
+// L2.  Slot indices and positions of 32 tokens sit one per lane, validated
+// once, and are fetched with a shuffle.  Math is fp32; the products of the
+// RMSNorm and of the rotation are rounded one by one, as in the definition.
 #include "kvq_launch.cuh"
 
 namespace kvq {
 namespace {
-
-constexpr int kStoreWarps = 4;
-constexpr int kStoreThreads = kStoreWarps * 32;
 
 struct StoreArgs {
     const uint8_t *x;
@@ -47,7 +49,20 @@ struct StoreArgs {
     uint8_t *pool;
     int64_t pool_slots;
     int32_t *err;
+    // token ranges (set by partition()): per_warp tokens per warp, one more
+    // for the first extra + skew warps, one fewer for the last skew warps
+    int64_t per_warp;
+    int64_t extra;
+    int64_t skew;
+    int64_t warps;
 };
+
+// Token range [start, start + cnt) of warp gw (see StoreArgs).
+__device__ __forceinline__ void token_range(const StoreArgs &a, int64_t gw, int64_t &start, int &cnt) {
+    const int64_t e1 = a.extra + a.skew, w2 = a.warps - a.skew;
+    start = gw * a.per_warp + (gw < e1 ? gw : e1) - (gw > w2 ? gw - w2 : 0);
+    cnt = int(a.per_warp) + (gw < e1 ? 1 : 0) - (gw >= w2 ? 1 : 0);
+}
 
 // 16-byte chunk position of (block, sub-chunk) inside a row: the sub-chunks
 // of a block are rotated so that eight lanes reading sub-chunk j of eight
@@ -105,14 +120,14 @@ __device__ __forceinline__ void block_amax(float (&v)[K][E], float (&am)[K]) {
     constexpr int LPB = kBlock / E;
 #pragma unroll
     for (int k = K0; k < K1; ++k) {
-        float m[E / 2];
-#pragma unroll
-        for (int e = 0; e < E / 2; ++e) m[e] = fmaxf(fabsf(v[k][2 * e]), fabsf(v[k][2 * e + 1]));
-#pragma unroll
-        for (int w = E / 4; w >= 1; w >>= 1)
-#pragma unroll
-            for (int e = 0; e < w; ++e) m[e] = fmaxf(m[e], m[e + w]);
-        float mm = m[0];
+        float mm;
+        if constexpr (E == 8) {
+            const float t0 = fmax3(fabsf(v[k][0]), fabsf(v[k][1]), fabsf(v[k][2]));
+            const float t1 = fmax3(fabsf(v[k][3]), fabsf(v[k][4]), fabsf(v[k][5]));
+            mm = fmax3(t0, t1, fmaxf(fabsf(v[k][6]), fabsf(v[k][7])));
+        } else {
+            mm = fmaxf(fmax3(fabsf(v[k][0]), fabsf(v[k][1]), fabsf(v[k][2])), fabsf(v[k][3]));
+        }
 #pragma unroll
         for (int off = 1; off < LPB; off <<= 1) mm = fmaxf(mm, __shfl_xor_sync(0xffffffffu, mm, off));
         am[k] = mm;
@@ -183,7 +198,7 @@ __device__ __forceinline__ void round_chunks(float (&v)[K][E]) {
 }
 
 template <Layout L, int PageBits, bool kBf16, bool kLoc64, bool kNorm, bool kRope, int kWarps>
-__global__ void __launch_bounds__(32 * kWarps, 8 * (kStoreWarps / kWarps)) store_warp_kernel(const StoreArgs a) {
+__global__ void __launch_bounds__(32 * kWarps, 32 / kWarps) store_warp_kernel(const StoreArgs a) {
     using SM = WarpStoreSmem<kBf16, kRope>;
     constexpr int D = SM::D, NS = SM::NS;
     constexpr int E = kBf16 ? 8 : 4;          // values per 16-byte chunk
@@ -197,10 +212,10 @@ __global__ void __launch_bounds__(32 * kWarps, 8 * (kStoreWarps / kWarps)) store
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     uint8_t *wsm = smem + warp * SM::kWarpBytes;
-    const int64_t W = int64_t(gridDim.x) * kWarps;
     const int64_t gw = int64_t(blockIdx.x) * kWarps + warp;
-    const int64_t start = a.n * gw / W;
-    const int cnt = int(a.n * (gw + 1) / W - start);
+    int64_t start;
+    int cnt;
+    token_range(a, gw, start, cnt);
 
     // While the upstream grid drains: pull this warp's first NS rows and its
     // slot / position lines into L2 (hints only; the loads come after the wait).
@@ -211,6 +226,26 @@ __global__ void __launch_bounds__(32 * kWarps, 8 * (kStoreWarps / kWarps)) store
         if constexpr (kRope) prefetch_l2(a.pos + start);
     }
     pdl_wait();
+
+    // Without RoPE the rows of the first D tokens are requested before the
+    // slot loads (which are waited for only when first used); with RoPE the
+    // first copies wait for the positions (measured at 16384 tokens: each
+    // order is the faster one for its instance).
+    const uint8_t *src_next = a.x + start * a.row_stride_bytes + lane * 16;
+    int ring_in = 0;
+    if constexpr (!kRope) {
+#pragma unroll
+        for (int j = 0; j < D; ++j) {
+            if (j < cnt) {
+                uint8_t *slot = wsm + ring_in * SM::SLOT + lane * 16;
+#pragma unroll
+                for (int k = 0; k < K; ++k) cp_async16(slot + k * 512, src_next + k * 512);
+                src_next += a.row_stride_bytes;
+                ring_in = (ring_in + 1) & (NS - 1);
+            }
+            cp_async_commit();
+        }
+    }
 
     // Slot / position of tokens 32b .. 32b+31 of this warp, one per lane,
     // validated once: an out-of-range slot or position becomes -1.
@@ -237,8 +272,6 @@ __global__ void __launch_bounds__(32 * kWarps, 8 * (kStoreWarps / kWarps)) store
     // Copies of token j into the next ring slot: one commit group for the
     // row and, with RoPE, a second one for its cos/sin values (which wait on
     // the position), so the rest of the row can be finished while they land.
-    const uint8_t *src_next = a.x + start * a.row_stride_bytes + lane * 16;
-    int ring_in = 0;
     auto issue = [&](int j) {
         if (j < cnt) {
             uint8_t *slot = wsm + ring_in * SM::SLOT + lane * 16;
@@ -289,18 +322,19 @@ __global__ void __launch_bounds__(32 * kWarps, 8 * (kStoreWarps / kWarps)) store
     if (kRope && cnt > 1) {
         // Let the first row land before asking for the next ones: every warp
         // starts at once, and behind the position -> cos/sin chain the first
-        // row is what holds the warp up (store + RoPE at 16384 tokens:
-        // 6.44 -> 6.26 us).  Warps with a single token, and the plain store,
-        // are faster without the wait.
+        // row is what holds the warp up.  Warps with a single token are
+        // faster without the wait.
         issue(0);
         pdl_trigger();
         cp_async_wait<kGroups - 1>();
 #pragma unroll
         for (int j = 1; j < D; ++j) issue(j);
-    } else {
+    } else if constexpr (kRope) {
 #pragma unroll
         for (int j = 0; j < D; ++j) issue(j);
         pdl_trigger();
+    } else {
+        pdl_trigger();  // the first rows went out above
     }
 
     int ring_out = 0;
@@ -351,7 +385,8 @@ __global__ void __launch_bounds__(32 * kWarps, 8 * (kStoreWarps / kWarps)) store
                     const int j = (kk * E / 2 + e / 2) & 3;
                     ss2[j] = ffma2(t, t, ss2[j]);
                 }
-            float ss = ((ss2[0].x + ss2[0].y) + (ss2[1].x + ss2[1].y)) + ((ss2[2].x + ss2[2].y) + (ss2[3].x + ss2[3].y));
+            const float2 s4 = fadd2(fadd2(ss2[0], ss2[1]), fadd2(ss2[2], ss2[3]));
+            float ss = s4.x + s4.y;
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
             const float ms = ss * (1.0f / kD);
@@ -413,8 +448,50 @@ __global__ void __launch_bounds__(32 * kWarps, 8 * (kStoreWarps / kWarps)) store
     cp_async_wait<0>();
 }
 
+// Round v[0..N) to bf16 (ties to even), in place.
+template <int N>
+__device__ __forceinline__ void round_bf16_n(float *v) {
+#pragma unroll
+    for (int e = 0; e < N; e += 2) {
+        const uint32_t b = pack_bf16x2(v[e], v[e + 1]);
+        v[e] = bf16_lo(b);
+        v[e + 1] = bf16_hi(b);
+    }
+}
+
+// max |v[i]| over 32 values (three-operand max: 16 instructions).
+__device__ __forceinline__ float amax32(const float *v) {
+    float m[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        float t = fmax3(fabsf(v[8 * q]), fabsf(v[8 * q + 1]), fabsf(v[8 * q + 2]));
+        t = fmax3(t, fabsf(v[8 * q + 3]), fabsf(v[8 * q + 4]));
+        t = fmax3(t, fabsf(v[8 * q + 5]), fabsf(v[8 * q + 6]));
+        m[q] = fmaxf(t, fabsf(v[8 * q + 7]));
+    }
+    return fmaxf(fmax3(m[0], m[1], m[2]), m[3]);
+}
+
+// Four V41 codes of x * mult (mult = 2^(127 - byte)), low byte first.
+__device__ __forceinline__ uint32_t v41_word(const float *x, float mult) {
+    const float2 a = fmul2(make_float2(x[0], x[1]), make_float2(mult, mult));
+    const float2 b = fmul2(make_float2(x[2], x[3]), make_float2(mult, mult));
+    return cvt_e4m3x2(a.x, a.y) | (cvt_e4m3x2(b.x, b.y) << 16);
+}
+
+// Eight e2m1 codes of x * inv, low nibble first.
+__device__ __forceinline__ uint32_t fp4_word(const float *x, float inv) {
+    uint32_t w = 0;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const float2 y = fmul2(make_float2(x[2 * q], x[2 * q + 1]), make_float2(inv, inv));
+        w |= cvt_e2m1x2(y.x, y.y) << (8 * q);
+    }
+    return w;
+}
+
 template <bool kBf16, bool kRope, bool kNorm>
-struct PairStoreSmem {
+struct StoreSmem {
     static constexpr int E = kBf16 ? 8 : 4;             // values per 16-byte chunk
     static constexpr int SUBS = kBlock / E;             // chunks per quant block
     static constexpr int CPR = kD / E;                  // chunks per row
@@ -425,35 +502,42 @@ struct PairStoreSmem {
     static_assert((NS & (NS - 1)) == 0, "ring index by mask");
     static constexpr int SLOT = 2 * XB + 2 * CSB;
     static constexpr int kWarpBytes = NS * SLOT;
-    static constexpr int kW = kStoreWarps * kWarpBytes;  // norm weights, swizzled
-    static constexpr int kBytes = kW + (kNorm ? kD * 4 : 0);
+    static constexpr int kWBytes = kNorm ? kD * 4 : 0;  // the norm weights, once per CTA
+    static constexpr int bytes(int warps) { return kWBytes + warps * kWarpBytes; }
     static_assert(SLOT % 16 == 0, "16-byte aligned slots");
     static_assert((2 * CPR) % 32 == 0, "a pair is whole chunks per lane");
 };
 
-template <Layout L, int PageBits, bool kBf16, bool kLoc64, bool kNorm, bool kRope>
-__global__ void __launch_bounds__(kStoreThreads, 4) store_pair_kernel(const StoreArgs a) {
-    using SM = PairStoreSmem<kBf16, kRope, kNorm>;
+template <Layout L, int PageBits, bool kBf16, bool kLoc64, bool kNorm, bool kRope, int kWarps>
+__global__ void __launch_bounds__(32 * kWarps, 16 / kWarps) store_half_kernel(const StoreArgs a) {
+    using SM = StoreSmem<kBf16, kRope, kNorm>;
     using PK = PagedKV<L, PageBits>;
     using T = LayoutTraits<L>;
     constexpr int D = SM::D, NS = SM::NS, E = SM::E, SUBS = SM::SUBS, CPR = SM::CPR;
-    constexpr int NC = 2 * CPR / 32;          // chunks each lane copies per pair
-    constexpr int kRopeBlk0 = kRopeStart / kBlock;  // first rotated block (14)
-    static_assert(kRopeD == 2 * kBlock, "the rotated dims are the last two blocks");
+    constexpr int NC = 2 * CPR / 32;                 // chunks each lane copies per pair
+    constexpr int kRopeBlk0 = kRopeStart / kBlock;   // first rotated block (14)
+    constexpr int kOwn = kRope ? kRopeBlk0 : kNBlk;  // lanes that own a whole block
+    static_assert(kRopeD == 2 * kBlock && kRopeD / 4 == 16, "the rotated dims are 16 quads, two blocks");
     static_assert(D < 16, "a pair's slot index is in the current or the next batch of 32");
+    // values after the fp32 math are rounded to bf16; a bf16 row without the
+    // norm keeps its (already bf16) non-rotated values as they are
+    constexpr bool kRoundBlk = kNorm || (kRope && !kBf16);
+    constexpr bool kRoundQuad = kNorm || kRope;
 
     extern __shared__ __align__(16) uint8_t smem[];
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int h = lane >> 4;   // token of the pair
-    const int bi = lane & 15;  // quant block owned
-    uint8_t *wsm = smem + warp * SM::kWarpBytes;
-    const float *s_w = reinterpret_cast<const float *>(smem + SM::kW);
-    const int64_t W = int64_t(gridDim.x) * kStoreWarps;
-    const int64_t gw = int64_t(blockIdx.x) * kStoreWarps + warp;
-    const int64_t start = a.n * gw / W;
-    const int cnt = int(a.n * (gw + 1) / W - start);
+    const int bi = lane & 15;  // quant block owned (and, with RoPE, rotated quad)
+    const float *s_w = reinterpret_cast<const float *>(smem);
+    uint8_t *wsm = smem + SM::kWBytes + warp * SM::kWarpBytes;
+    const int64_t gw = int64_t(blockIdx.x) * kWarps + warp;
+    int64_t start;
+    int cnt;
+    token_range(a, gw, start, cnt);
     const int npairs = (cnt + 1) >> 1;
+    // 32-byte code stores need a 32-byte aligned pool (the ABI asks for 16)
+    const bool pool32 = (reinterpret_cast<uintptr_t>(a.pool) & 31) == 0;
 
     // While the upstream grid drains: L2 hints for this warp's first NS pairs
     // and its slot / position lines (the loads come after the wait).
@@ -465,12 +549,45 @@ __global__ void __launch_bounds__(kStoreThreads, 4) store_pair_kernel(const Stor
     }
     pdl_wait();
 
+    // With RoPE the first pair's rows go out before anything that could
+    // stall the warp, and the pairs' cos/sin rows are commit groups of their
+    // own (they wait on the positions), so that the non-rotated blocks are
+    // finished while they land: kG groups per pair, rows then cos/sin.
+    // Without RoPE the first pair is requested after the slot loads (both
+    // orders measured at 16384 tokens: each is the faster one for its
+    // instance).
+    constexpr int kG = kRope ? 2 : 1;  // commit groups per pair
+    int ring_in = 0;
+    const uint8_t *xw = a.x + start * a.row_stride_bytes;  // this warp's first row
+    auto issue_rows = [&](int p) {
+        if (p < npairs) {
+            uint8_t *slot = wsm + ring_in * SM::SLOT;
+            const uint8_t *r0 = xw + int64_t(2 * p) * a.row_stride_bytes;
+#pragma unroll
+            for (int m = 0; m < NC; ++m) {
+                constexpr int kPerRow = CPR / 32;          // copy instructions per row
+                const int r = m / kPerRow;                 // token of the pair (compile-time)
+                const int cc = 32 * (m % kPerRow) + lane;  // chunk in the row
+                if (2 * p + r < cnt)
+                    cp_async16(slot + (r * CPR + swz<SUBS>(cc / SUBS, cc % SUBS)) * 16,
+                               r0 + r * a.row_stride_bytes + cc * 16);
+            }
+            ring_in = (ring_in + 1) & (NS - 1);
+        }
+        cp_async_commit();
+    };
+    if constexpr (kRope) issue_rows(0);
+
     if constexpr (kNorm) {  // the weight row, block-swizzled like fp32 rows
-        float *w = reinterpret_cast<float *>(smem + SM::kW);
-        for (int c = threadIdx.x; c < kD / 4; c += kStoreThreads)
+        float *w = reinterpret_cast<float *>(smem);
+        for (int c = threadIdx.x; c < kD / 4; c += 32 * kWarps)
             *reinterpret_cast<float4 *>(w + 4 * swz<8>(c >> 3, c & 7)) =
                 __ldg(reinterpret_cast<const float4 *>(a.w) + c);
-        __syncthreads();
+        if constexpr (kWarps > 1) {
+            __syncthreads();
+        } else {
+            __syncwarp();
+        }
     }
 
     // Slot / position of tokens 32b .. 32b+31 of this warp, one per lane,
@@ -495,42 +612,35 @@ __global__ void __launch_bounds__(kStoreThreads, 4) store_pair_kernel(const Stor
     }
     int cur_b = 0;
 
-    // copies of token pair p (tokens 2p, 2p+1) into the next ring slot
-    int ring_in = 0;
-    auto issue = [&](int p) {
-        if (p < npairs) {
-            uint8_t *slot = wsm + ring_in * SM::SLOT;
-#pragma unroll
-            for (int m = 0; m < NC; ++m) {
-                const int c = lane + 32 * m;
-                const int r = c / CPR, cc = c % CPR;
-                if (2 * p + r < cnt)
-                    cp_async16(slot + (r * CPR + swz<SUBS>(cc / SUBS, cc % SUBS)) * 16,
-                               a.x + (start + 2 * p + r) * a.row_stride_bytes + cc * 16);
-            }
-            if constexpr (kRope) {
-                const int t = 2 * p + h;
-                const int32_t pt = __shfl_sync(0xffffffffu, (t >> 5) == cur_b ? p_cur : p_nxt, t & 31);
-                if (t < cnt && pt >= 0)
-                    cp_async16(slot + 2 * SM::XB + h * SM::CSB + bi * 16, a.cs + int64_t(pt) * kRopeD + bi * 4);
-            }
-            ring_in = (ring_in + 1) & (NS - 1);
+    auto issue_cs = [&](int p) {
+        if constexpr (kRope) {
+            const int t = 2 * p + h;
+            const int32_t pt = __shfl_sync(0xffffffffu, (t >> 5) == cur_b ? p_cur : p_nxt, t & 31);
+            if (t < cnt && pt >= 0)
+                cp_async16(wsm + (p & (NS - 1)) * SM::SLOT + 2 * SM::XB + h * SM::CSB + bi * 16,
+                           a.cs + int64_t(pt) * kRopeD + bi * 4);
+            cp_async_commit();
         }
-        cp_async_commit();
     };
-
+    auto issue = [&](int p) {
+        issue_rows(p);
+        issue_cs(p);
+    };
+    if constexpr (kRope) {
+        issue_cs(0);
+    } else {
+        issue_rows(0);
+    }
     if (npairs > 1) {
         // The first pair lands before the next ones are requested: every warp
-        // starts at once, and the first pair is what holds it up (FP4 store
-        // at 16384 tokens: 5.07 -> 4.82 us).
-        issue(0);
+        // starts at once, and the first pair is what holds it up.
         pdl_trigger();
-        cp_async_wait<0>();
+        cp_async_wait<kG - 1>();
 #pragma unroll
         for (int p = 1; p < D; ++p) issue(p);
     } else {
 #pragma unroll
-        for (int p = 0; p < D; ++p) issue(p);
+        for (int p = 1; p < D; ++p) issue(p);
         pdl_trigger();
     }
 
@@ -545,31 +655,51 @@ __global__ void __launch_bounds__(kStoreThreads, 4) store_pair_kernel(const Stor
                 if constexpr (kRope) p_nxt = ld_pos(2 * k + 32 + lane);
             }
         }
-        cp_async_wait<D - 1>();  // this lane's copies of pair k have landed ...
-        __syncwarp();            // ... and so have the other lanes'
+        cp_async_wait<kG * D - 1>();  // this lane's row copies of pair k have landed ...
+        __syncwarp();                 // ... and so have the other lanes'
         const uint8_t *slot_sm = wsm + ring_out * SM::SLOT;
         ring_out = (ring_out + 1) & (NS - 1);
+        const uint8_t *row = slot_sm + h * SM::XB;
 
+        // this lane's block (lanes 14 and 15 read the rotated blocks, unused with RoPE)
         float v[kBlock];
-        {
-            const uint8_t *row = slot_sm + h * SM::XB;
 #pragma unroll
-            for (int j = 0; j < SUBS; ++j) unpack_chunk<kBf16>(lds_u4(row + swz<SUBS>(bi, j) * 16), v + j * E);
+        for (int j = 0; j < SUBS; ++j) unpack_chunk<kBf16>(lds_u4(row + swz<SUBS>(bi, j) * 16), v + j * E);
+        // with RoPE: this lane's quad of rotated dims
+        float qv[4] = {0.f, 0.f, 0.f, 0.f};
+        if constexpr (kRope) {
+            const int blk = kRopeBlk0 + (bi >> 3);
+            const int off = (4 * bi) & (kBlock - 1);  // first value of the quad inside its block
+            const uint8_t *qp = row + swz<SUBS>(blk, off / E) * 16 + (off % E) * (kBf16 ? 2 : 4);
+            if constexpr (kBf16) {
+                const uint2 r = lds_u2(qp);
+                qv[0] = bf16_lo(r.x), qv[1] = bf16_hi(r.x), qv[2] = bf16_lo(r.y), qv[3] = bf16_hi(r.y);
+            } else {
+                const uint4 r = lds_u4(qp);
+                qv[0] = __uint_as_float(r.x), qv[1] = __uint_as_float(r.y);
+                qv[2] = __uint_as_float(r.z), qv[3] = __uint_as_float(r.w);
+            }
         }
         const int t = 2 * k + h;
         const bool active = t < cnt;
         const int32_t slot = __shfl_sync(0xffffffffu, sl_cur, t & 31);
         int32_t pt = 0;
         if constexpr (kRope) pt = __shfl_sync(0xffffffffu, p_cur, t & 31);
+        issue(k + D);  // refill the ring (the slot of pair k-1) while this pair is computed
 
         if constexpr (kNorm) {
-            float2 ss2 = make_float2(0.f, 0.f);
+            float2 sa = make_float2(0.f, 0.f), sb = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int e = 0; e < kBlock; e += 2) {
-                const float2 t2 = make_float2(v[e], v[e + 1]);
-                ss2 = ffma2(t2, t2, ss2);
+            for (int e = 0; e < kBlock; e += 4) {
+                sa = ffma2(make_float2(v[e], v[e + 1]), make_float2(v[e], v[e + 1]), sa);
+                sb = ffma2(make_float2(v[e + 2], v[e + 3]), make_float2(v[e + 2], v[e + 3]), sb);
             }
-            float ss = ss2.x + ss2.y;
+            float ss = bi < kOwn ? (sa.x + sa.y) + (sb.x + sb.y) : 0.f;
+            if constexpr (kRope) {
+                const float2 qa = fmul2(make_float2(qv[0], qv[1]), make_float2(qv[0], qv[1]));
+                const float2 qb = ffma2(make_float2(qv[2], qv[3]), make_float2(qv[2], qv[3]), qa);
+                ss += qb.x + qb.y;
+            }
 #pragma unroll
             for (int off = 8; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
             const float inv = rsqrt_approx(__fadd_rn(ss * (1.0f / kD), a.eps));
@@ -579,135 +709,164 @@ __global__ void __launch_bounds__(kStoreThreads, 4) store_pair_kernel(const Stor
                 const float4 wv = *reinterpret_cast<const float4 *>(s_w + 4 * swz<8>(bi, j));
                 const float2 a0 = fmul2(fmul2(make_float2(v[4 * j], v[4 * j + 1]), inv2), make_float2(wv.x, wv.y));
                 const float2 a1 = fmul2(fmul2(make_float2(v[4 * j + 2], v[4 * j + 3]), inv2), make_float2(wv.z, wv.w));
-                v[4 * j] = a0.x;
-                v[4 * j + 1] = a0.y;
-                v[4 * j + 2] = a1.x;
-                v[4 * j + 3] = a1.y;
+                v[4 * j] = a0.x, v[4 * j + 1] = a0.y, v[4 * j + 2] = a1.x, v[4 * j + 3] = a1.y;
+            }
+            if constexpr (kRope) {
+                const float4 wq = *reinterpret_cast<const float4 *>(s_w + 4 * swz<8>(kRopeBlk0 + (bi >> 3), bi & 7));
+                const float2 a0 = fmul2(fmul2(make_float2(qv[0], qv[1]), inv2), make_float2(wq.x, wq.y));
+                const float2 a1 = fmul2(fmul2(make_float2(qv[2], qv[3]), inv2), make_float2(wq.z, wq.w));
+                qv[0] = a0.x, qv[1] = a0.y, qv[2] = a1.x, qv[3] = a1.y;
             }
         }
-        if constexpr (kRope) {
-            if (bi >= kRopeBlk0) {  // pairs (bi - 14) * 16 .. +15 of the rotation
-                const float *cs = reinterpret_cast<const float *>(slot_sm + 2 * SM::XB + h * SM::CSB);
-                const int q0 = (bi - kRopeBlk0) * (kBlock / 2);
-#pragma unroll
-                for (int g = 0; g < kBlock / 8; ++g) {
-                    const float4 c4 = *reinterpret_cast<const float4 *>(cs + q0 + 4 * g);
-                    const float4 s4 = *reinterpret_cast<const float4 *>(cs + kRopeD / 2 + q0 + 4 * g);
-                    const float cc[4] = {c4.x, c4.y, c4.z, c4.w}, sn[4] = {s4.x, s4.y, s4.z, s4.w};
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const float2 xv = make_float2(v[8 * g + 2 * q], v[8 * g + 2 * q + 1]);
-                        const float2 p = fmul2(xv, make_float2(cc[q], sn[q]));  // (a*c, b*s)
-                        const float2 r = fmul2(xv, make_float2(sn[q], cc[q]));  // (a*s, b*c)
-                        v[8 * g + 2 * q] = __fsub_rn(p.x, p.y);
-                        v[8 * g + 2 * q + 1] = __fadd_rn(r.x, r.y);
-                    }
-                }
-            }
-        }
-        issue(k + D);  // refill the ring while this pair is computed
 
-        if constexpr (kNorm || kRope) {
-#pragma unroll
-            for (int e = 0; e < kBlock; e += 2) {
-                const uint32_t b = pack_bf16x2(v[e], v[e + 1]);
-                v[e] = bf16_lo(b);
-                v[e + 1] = bf16_hi(b);
-            }
-        }
-        // block absmax (this lane holds the whole block): four running maxima
-        float m0 = fabsf(v[0]), m1 = fabsf(v[1]), m2 = fabsf(v[2]), m3 = fabsf(v[3]);
-#pragma unroll
-        for (int e = 4; e < kBlock; e += 4) {
-            m0 = fmaxf(m0, fabsf(v[e]));
-            m1 = fmaxf(m1, fabsf(v[e + 1]));
-            m2 = fmaxf(m2, fabsf(v[e + 2]));
-            m3 = fmaxf(m3, fabsf(v[e + 3]));
-        }
-        const uint32_t amax = __float_as_uint(fmaxf(fmaxf(m0, m1), fmaxf(m2, m3)));
-
+        // the blocks this lane owns: round, absmax, quantise, store
+        if constexpr (kRoundBlk) round_bf16_n<kBlock>(v);
+        const float am = amax32(v);
         const bool bad_pos = kRope && pt < 0;
-        if (!active || bad_pos || slot < 0) {
-            if (active && bi == 0) raise_err(a.err, bad_pos ? KVQ_DEVERR_POS : KVQ_DEVERR_SLOT);
-            continue;
-        }
-        const int64_t page = int64_t(slot >> PageBits) * PK::kPageBytes;
-        const int row = slot & int(PK::kPage - 1);
-        uint8_t *crow = a.pool + page + row * T::kCodeBytes;
-        uint8_t *srow = a.pool + page + PK::kPage * T::kCodeBytes + row * T::kScaleBytes;
-        uint32_t sbyte;
-        if constexpr (L == Layout::V41) {
-            sbyte = v41_scale_byte(amax);
-            const float mult = v41_multiplier(sbyte);
-            const float2 mult2 = make_float2(mult, mult);
-            uint32_t wd[8];
+        const bool ok = active && !bad_pos && slot >= 0;
+        if (active && !ok && bi == 0) raise_err(a.err, bad_pos ? KVQ_DEVERR_POS : KVQ_DEVERR_SLOT);
+        uint8_t *crow = nullptr, *srow = nullptr;
+        if (ok) {
+            const int64_t page = int64_t(slot >> PageBits) * PK::kPageBytes;
+            const int row_i = slot & int(PK::kPage - 1);
+            crow = a.pool + page + row_i * T::kCodeBytes;
+            srow = a.pool + page + PK::kPage * T::kCodeBytes + row_i * T::kScaleBytes;
+            if constexpr (L == Layout::V41) {
+                const uint32_t sbyte = v41_scale_byte(__float_as_uint(am));
+                const float mult = v41_multiplier(sbyte);
+                if (bi < kOwn) {
+                    uint32_t wd[8];
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const float2 lo = fmul2(make_float2(v[4 * q], v[4 * q + 1]), mult2);
-                const float2 hi = fmul2(make_float2(v[4 * q + 2], v[4 * q + 3]), mult2);
-                wd[q] = cvt_e4m3x2(lo.x, lo.y) | (cvt_e4m3x2(hi.x, hi.y) << 16);
+                    for (int q = 0; q < 8; ++q) wd[q] = v41_word(v + 4 * q, mult);
+                    if (pool32) {
+                        st_v8(crow + bi * 32, wd);
+                    } else {
+                        st_u4(crow + bi * 32, make_uint4(wd[0], wd[1], wd[2], wd[3]));
+                        st_u4(crow + bi * 32 + 16, make_uint4(wd[4], wd[5], wd[6], wd[7]));
+                    }
+                    srow[bi] = uint8_t(sbyte);
+                }
+            } else {
+                const uint32_t sbyte = fp4_scale_byte(__float_as_uint(am));
+                if (bi < kOwn) {
+                    const float S = e4m3x2_to_f32x2(sbyte).x;
+                    const float inv = __frcp_rn(S);
+                    uint32_t wd[4] = {0u, 0u, 0u, 0u};
+                    if (S != 0.0f) {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) wd[q] = fp4_word(v + 8 * q, inv);
+                    }
+                    st_u4(crow + bi * 16, make_uint4(wd[0], wd[1], wd[2], wd[3]));
+                    srow[bi] = uint8_t(sbyte);
+                }
+                if (bi == 0) st_u4(srow + 16, make_uint4(0u, 0u, 0u, 0u));
             }
-            st_u4(crow + bi * 32, make_uint4(wd[0], wd[1], wd[2], wd[3]));
-            st_u4(crow + bi * 32 + 16, make_uint4(wd[4], wd[5], wd[6], wd[7]));
-        } else {
-            sbyte = fp4_scale_byte(amax);
-            const float S = e4m3x2_to_f32x2(sbyte).x;
-            const float inv = __frcp_rn(S);
-            uint32_t wd[4] = {0u, 0u, 0u, 0u};
-            if (S != 0.0f) {
+        }
+
+        // the rotated quads, once this pair's cos/sin rows have landed
+        if constexpr (kRope) {
+            cp_async_wait<2 * D>();  // (a refill of two groups was committed since)
+            __syncwarp();
+            const uint8_t *cs = slot_sm + 2 * SM::XB + h * SM::CSB;
+            const uint2 cc = lds_u2(cs + 8 * bi), ss = lds_u2(cs + kRopeD * 2 + 8 * bi);
+            const float cq[2] = {__uint_as_float(cc.x), __uint_as_float(cc.y)};
+            const float sq[2] = {__uint_as_float(ss.x), __uint_as_float(ss.y)};
 #pragma unroll
-                for (int q = 0; q < 16; ++q) {
-                    const float2 y = fmul2(make_float2(v[2 * q], v[2 * q + 1]), make_float2(inv, inv));
-                    wd[q >> 2] |= cvt_e2m1x2(y.x, y.y) << (8 * (q & 3));
+            for (int q = 0; q < 2; ++q) {  // pairs 2i and 2i+1 of the rotation
+                const float2 xv = make_float2(qv[2 * q], qv[2 * q + 1]);
+                const float2 p = fmul2(xv, make_float2(cq[q], sq[q]));  // (a*c, b*s)
+                const float2 r = fmul2(xv, make_float2(sq[q], cq[q]));  // (a*s, b*c)
+                qv[2 * q] = __fsub_rn(p.x, p.y);
+                qv[2 * q + 1] = __fadd_rn(r.x, r.y);
+            }
+            if constexpr (kRoundQuad) round_bf16_n<4>(qv);
+            float amq = fmaxf(fmax3(fabsf(qv[0]), fabsf(qv[1]), fabsf(qv[2])), fabsf(qv[3]));
+#pragma unroll
+            for (int off = 4; off > 0; off >>= 1) amq = fmaxf(amq, __shfl_xor_sync(0xffffffffu, amq, off));
+            if (ok) {
+                if constexpr (L == Layout::V41) {
+                    const uint32_t sbq = v41_scale_byte(__float_as_uint(amq));
+                    *reinterpret_cast<uint32_t *>(crow + kRopeStart + 4 * bi) = v41_word(qv, v41_multiplier(sbq));
+                    if ((bi & 7) == 0) srow[kRopeBlk0 + (bi >> 3)] = uint8_t(sbq);
+                } else {
+                    const uint32_t sbq = fp4_scale_byte(__float_as_uint(amq));
+                    const float S = e4m3x2_to_f32x2(sbq).x;
+                    const float inv = __frcp_rn(S);
+                    uint32_t w2 = 0;
+                    if (S != 0.0f) {
+                        const float2 y0 = fmul2(make_float2(qv[0], qv[1]), make_float2(inv, inv));
+                        const float2 y1 = fmul2(make_float2(qv[2], qv[3]), make_float2(inv, inv));
+                        w2 = cvt_e2m1x2(y0.x, y0.y) | (cvt_e2m1x2(y1.x, y1.y) << 8);
+                    }
+                    *reinterpret_cast<uint16_t *>(crow + kRopeStart / 2 + 2 * bi) = uint16_t(w2);
+                    if ((bi & 7) == 0) srow[kRopeBlk0 + (bi >> 3)] = uint8_t(sbq);
                 }
             }
-            st_u4(crow + bi * 16, make_uint4(wd[0], wd[1], wd[2], wd[3]));
-            if (bi == 0) st_u4(srow + 16, make_uint4(0u, 0u, 0u, 0u));
         }
-        srow[bi] = uint8_t(sbyte);
     }
     cp_async_wait<0>();
 }
 
-// V41 rows use the warp-per-token kernel (fewer instructions for the
-// norm / RoPE paths); V41_FP4 rows use the pair kernel, which computes each
-// block's e4m3 scale and its reciprocal once per block instead of once per
-// lane of the block.
+// Contiguous token ranges for `warps` warps, computed on the host so that no
+// warp divides.  The first warps take the remainder: when a launch follows
+// another under PDL, the lowest CTAs become resident (and prefetch) first,
+// so front-loading them evens out the finish times.  `skew` moves one more
+// token from each of the last `skew` warps to the first ones (only when
+// every warp holds four tokens or more).
+inline StoreArgs partition(const StoreArgs &a, int64_t warps, int64_t skew) {
+    StoreArgs b = a;
+    b.warps = warps;
+    b.per_warp = a.n / warps;
+    b.extra = a.n % warps;
+    if (b.per_warp < 4) skew = 0;  // small batches: one pair per warp is the latency
+    if (b.extra + 2 * skew > warps) skew = (warps - b.extra) / 2;
+    b.skew = skew;
+    return b;
+}
+
+template <auto Kernel, int Warps, size_t Smem>
+kvq_status launch_persistent(const StoreArgs &a, int64_t tokens_per_warp, int skew_div, cudaStream_t stream) {
+    int64_t cap = 0;
+    kvq_status st = resident_grid<Kernel, 32 * Warps>(Smem, &cap);
+    if (st != KVQ_OK) return st;
+    const int64_t want = (a.n + tokens_per_warp * Warps - 1) / (tokens_per_warp * Warps);
+    const int64_t grid = want < cap ? want : cap;
+    const int64_t warps = grid * Warps;
+    return launch_pdl_smem(Kernel, dim3(unsigned(grid)), dim3(32 * Warps), Smem, stream,
+                           partition(a, warps, skew_div > 0 ? warps / skew_div : 0));
+}
+
+// Which kernel serves which instance (each choice measured at 16384 tokens):
+//  * V41 without RoPE, and the fused norm + RoPE: one warp per token.  The
+//    norm + RoPE instance launches one-warp CTAs from three tokens per
+//    resident warp up, so that a finished warp frees its slot at once and
+//    the next launch's warps become resident (and prefetch) sooner; with
+//    fewer tokens per warp the four times larger CTA count costs more in
+//    dispatch than it saves.
+//  * V41 with RoPE only: the half-warp kernel (the rotation spread over all
+//    16 lanes), one-warp CTAs, half the warps' remainder front-loaded.
+//  * V41_FP4: the half-warp kernel (each block's e4m3 scale, division and
+//    reciprocal computed once), four-warp CTAs.
 template <Layout L, int PB, bool B16, bool L64, bool N, bool R>
 kvq_status launch_store(const StoreArgs &a, cudaStream_t stream) {
-    if constexpr (L == Layout::V41) {
+    if constexpr (L == Layout::V41 && !(R && !N)) {
         constexpr size_t wsm = WarpStoreSmem<B16, R>::kWarpBytes;
-        constexpr auto kern4 = store_warp_kernel<L, PB, B16, L64, N, R, kStoreWarps>;
-        int64_t cap4 = 0;
-        kvq_status st = resident_grid<kern4, kStoreThreads>(kStoreWarps * wsm, &cap4);
-        if (st != KVQ_OK) return st;
+        constexpr auto kern4 = store_warp_kernel<L, PB, B16, L64, N, R, 4>;
         if constexpr (N && R) {
-            // The fused norm + RoPE instance also has a one-warp-CTA form.
-            // With each warp holding at least three tokens, a finished warp
-            // then frees its slot at once, so the next launch's warps become
-            // resident, and start their L2 prefetch, sooner (norm + RoPE at
-            // 16384 tokens: 7.45 -> 7.15 us).  With fewer tokens per warp the
-            // four times larger CTA count costs more in dispatch than it
-            // saves (2.97 -> 5.56 us at 4096 tokens).
             constexpr auto kern1 = store_warp_kernel<L, PB, B16, L64, N, R, 1>;
-            int64_t cap1 = 0;
-            st = resident_grid<kern1, 32>(wsm, &cap1);
+            int64_t cap1 = 0, cap4 = 0;
+            kvq_status st = resident_grid<kern1, 32>(wsm, &cap1);
+            if (st == KVQ_OK) st = resident_grid<kern4, 128>(4 * wsm, &cap4);
             if (st != KVQ_OK) return st;
-            if (cap1 >= kStoreWarps * cap4 && a.n >= 3 * cap1)
-                return launch_pdl_smem(kern1, dim3(unsigned(cap1)), dim3(32), wsm, stream, a);
+            if (cap1 >= 4 * cap4 && a.n >= 3 * cap1) return launch_persistent<kern1, 1, wsm>(a, 1, 0, stream);
         }
-        const int64_t want = (a.n + kStoreWarps - 1) / kStoreWarps;
-        const int64_t grid = want < cap4 ? want : cap4;
-        return launch_pdl_smem(kern4, dim3(unsigned(grid)), dim3(kStoreThreads), kStoreWarps * wsm, stream, a);
+        return launch_persistent<kern4, 4, 4 * wsm>(a, 1, 0, stream);
+    } else if constexpr (L == Layout::V41) {
+        using SM = StoreSmem<B16, R, N>;
+        return launch_persistent<store_half_kernel<L, PB, B16, L64, N, R, 1>, 1, SM::bytes(1)>(a, 2, 2, stream);
     } else {
-        constexpr auto kern = store_pair_kernel<L, PB, B16, L64, N, R>;
-        constexpr size_t smem = PairStoreSmem<B16, R, N>::kBytes;
-        int64_t cap = 0;
-        kvq_status st = resident_grid<kern, kStoreThreads>(smem, &cap);
-        if (st != KVQ_OK) return st;
-        const int64_t want = (a.n + 2 * kStoreWarps - 1) / (2 * kStoreWarps);
-        const int64_t grid = want < cap ? want : cap;
-        return launch_pdl_smem(kern, dim3(unsigned(grid)), dim3(kStoreThreads), smem, stream, a);
+        using SM = StoreSmem<B16, R, N>;
+        return launch_persistent<store_half_kernel<L, PB, B16, L64, N, R, 4>, 4, SM::bytes(4)>(a, 2, 0, stream);
     }
 }
 
