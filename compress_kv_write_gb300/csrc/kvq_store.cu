@@ -211,7 +211,7 @@ __global__ void __launch_bounds__(32 * kWarps, 32 / kWarps) store_warp_kernel(co
     extern __shared__ __align__(16) uint8_t smem[];
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    uint8_t *wsm = smem + warp * SM::kWarpBytes;
+    const uint32_t wsm = smem_addr(smem) + warp * SM::kWarpBytes;  // this warp's ring (shared window)
     const int64_t gw = int64_t(blockIdx.x) * kWarps + warp;
     int64_t start;
     int cnt;
@@ -237,7 +237,7 @@ __global__ void __launch_bounds__(32 * kWarps, 32 / kWarps) store_warp_kernel(co
 #pragma unroll
         for (int j = 0; j < D; ++j) {
             if (j < cnt) {
-                uint8_t *slot = wsm + ring_in * SM::SLOT + lane * 16;
+                const uint32_t slot = wsm + ring_in * SM::SLOT + lane * 16;
 #pragma unroll
                 for (int k = 0; k < K; ++k) cp_async16(slot + k * 512, src_next + k * 512);
                 src_next += a.row_stride_bytes;
@@ -274,7 +274,7 @@ __global__ void __launch_bounds__(32 * kWarps, 32 / kWarps) store_warp_kernel(co
     // the position), so the rest of the row can be finished while they land.
     auto issue = [&](int j) {
         if (j < cnt) {
-            uint8_t *slot = wsm + ring_in * SM::SLOT + lane * 16;
+            const uint32_t slot = wsm + ring_in * SM::SLOT + lane * 16;
 #pragma unroll
             for (int k = 0; k < K; ++k) cp_async16(slot + k * 512, src_next + k * 512);
             if constexpr (kRope) {
@@ -283,7 +283,7 @@ __global__ void __launch_bounds__(32 * kWarps, 32 / kWarps) store_warp_kernel(co
                 if (lane >= kRopeLane0 && pj >= 0) {
                     const int i0 = ((K - 1) * 32 + lane) * E / 2 - kRopeStart / 2;
                     const float *cs = a.cs + int64_t(pj) * kRopeD;
-                    uint8_t *dst = wsm + ring_in * SM::SLOT + SM::XB + (lane - kRopeLane0) * E * 4;
+                    const uint32_t dst = wsm + ring_in * SM::SLOT + SM::XB + (lane - kRopeLane0) * E * 4;
                     if constexpr (E == 8) {
                         cp_async16(dst, cs + i0);
                         cp_async16(dst + 16, cs + kRopeD / 2 + i0);
@@ -350,7 +350,7 @@ __global__ void __launch_bounds__(32 * kWarps, 32 / kWarps) store_warp_kernel(co
         }
         // Token k's row has landed once at most kGroups * D - 1 groups are pending.
         cp_async_wait<kGroups * D - 1>();
-        const uint8_t *slot_sm = wsm + ring_out * SM::SLOT;
+        const uint32_t slot_sm = wsm + ring_out * SM::SLOT;
         ring_out = (ring_out + 1) & (NS - 1);
         uint4 raw[K];
 #pragma unroll
@@ -413,7 +413,7 @@ __global__ void __launch_bounds__(32 * kWarps, 32 / kWarps) store_warp_kernel(co
             cp_async_wait<2 * D>();  // ... and its cos/sin values (two groups were added since)
             if (lane >= kRopeLane0) {
                 float cosv[E / 2], sinv[E / 2];
-                const uint8_t *cs = slot_sm + SM::XB + (lane - kRopeLane0) * E * 4;
+                const uint32_t cs = slot_sm + SM::XB + (lane - kRopeLane0) * E * 4;
                 if constexpr (E == 8) {
                     const uint4 c4 = lds_u4(cs), s4 = lds_u4(cs + 16);
                     cosv[0] = __uint_as_float(c4.x), cosv[1] = __uint_as_float(c4.y);
@@ -421,9 +421,9 @@ __global__ void __launch_bounds__(32 * kWarps, 32 / kWarps) store_warp_kernel(co
                     sinv[0] = __uint_as_float(s4.x), sinv[1] = __uint_as_float(s4.y);
                     sinv[2] = __uint_as_float(s4.z), sinv[3] = __uint_as_float(s4.w);
                 } else {
-                    const float2 c2 = *reinterpret_cast<const float2 *>(cs);
-                    const float2 s2 = *reinterpret_cast<const float2 *>(cs + 8);
-                    cosv[0] = c2.x, cosv[1] = c2.y, sinv[0] = s2.x, sinv[1] = s2.y;
+                    const uint2 c2 = lds_u2(cs), s2 = lds_u2(cs + 8);
+                    cosv[0] = __uint_as_float(c2.x), cosv[1] = __uint_as_float(c2.y);
+                    sinv[0] = __uint_as_float(s2.x), sinv[1] = __uint_as_float(s2.y);
                 }
 #pragma unroll
                 for (int q = 0; q < E / 2; ++q) {
@@ -479,18 +479,38 @@ __device__ __forceinline__ uint32_t v41_word(const float *x, float mult) {
     return cvt_e4m3x2(a.x, a.y) | (cvt_e4m3x2(b.x, b.y) << 16);
 }
 
-// Eight e2m1 codes of x * inv, low nibble first.
+// Eight e2m1 codes of x * inv, low nibble first: four converted bytes
+// packed into one word by a single mov.
 __device__ __forceinline__ uint32_t fp4_word(const float *x, float inv) {
-    uint32_t w = 0;
+    float2 y[4];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        const float2 y = fmul2(make_float2(x[2 * q], x[2 * q + 1]), make_float2(inv, inv));
-        w |= cvt_e2m1x2(y.x, y.y) << (8 * q);
-    }
+    for (int q = 0; q < 4; ++q) y[q] = fmul2(make_float2(x[2 * q], x[2 * q + 1]), make_float2(inv, inv));
+    uint32_t w;
+    asm("{\n\t.reg .b8 t0, t1, t2, t3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 t0, %2, %1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 t1, %4, %3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 t2, %6, %5;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 t3, %8, %7;\n\t"
+        "mov.b32 %0, {t0, t1, t2, t3};\n\t}"
+        : "=r"(w)
+        : "f"(y[0].x), "f"(y[0].y), "f"(y[1].x), "f"(y[1].y), "f"(y[2].x), "f"(y[2].y), "f"(y[3].x),
+          "f"(y[3].y));
     return w;
 }
 
-template <bool kBf16, bool kRope, bool kNorm>
+// V41_FP4 block scale byte e4m3(fl(amax / 6)) with a two-FMA quotient in
+// place of a correctly rounded division: the quotient can differ from the
+// correctly rounded one in its last bit, but an exhaustive run over every
+// positive finite fp32 amax on the GB300 found the e4m3 byte identical in all
+// cases, so the stored scale is the one the definition gives.
+__device__ __forceinline__ uint32_t fp4_scale_byte_fast(float amax) {
+    const float c = __uint_as_float(0x3E2AAAABu);  // 1/6 rounded to nearest
+    const float q0 = __fmul_rn(amax, c);
+    const float q1 = __fmaf_rn(__fmaf_rn(-q0, 6.0f, amax), c, q0);
+    return cvt_e4m3x2(q1, 0.0f) & 0xFFu;
+}
+
+template <Layout L, bool kBf16, bool kRope, bool kNorm>
 struct StoreSmem {
     static constexpr int E = kBf16 ? 8 : 4;             // values per 16-byte chunk
     static constexpr int SUBS = kBlock / E;             // chunks per quant block
@@ -503,14 +523,15 @@ struct StoreSmem {
     static constexpr int SLOT = 2 * XB + 2 * CSB;
     static constexpr int kWarpBytes = NS * SLOT;
     static constexpr int kWBytes = kNorm ? kD * 4 : 0;  // the norm weights, once per CTA
-    static constexpr int bytes(int warps) { return kWBytes + warps * kWarpBytes; }
+    static constexpr int kRcpBytes = L == Layout::FP4 ? 128 * 4 : 0;  // 1/scale per e4m3 scale byte
+    static constexpr int bytes(int warps) { return kWBytes + kRcpBytes + warps * kWarpBytes; }
     static_assert(SLOT % 16 == 0, "16-byte aligned slots");
     static_assert((2 * CPR) % 32 == 0, "a pair is whole chunks per lane");
 };
 
 template <Layout L, int PageBits, bool kBf16, bool kLoc64, bool kNorm, bool kRope, int kWarps>
 __global__ void __launch_bounds__(32 * kWarps, 16 / kWarps) store_half_kernel(const StoreArgs a) {
-    using SM = StoreSmem<kBf16, kRope, kNorm>;
+    using SM = StoreSmem<L, kBf16, kRope, kNorm>;
     using PK = PagedKV<L, PageBits>;
     using T = LayoutTraits<L>;
     constexpr int D = SM::D, NS = SM::NS, E = SM::E, SUBS = SM::SUBS, CPR = SM::CPR;
@@ -530,7 +551,8 @@ __global__ void __launch_bounds__(32 * kWarps, 16 / kWarps) store_half_kernel(co
     const int h = lane >> 4;   // token of the pair
     const int bi = lane & 15;  // quant block owned (and, with RoPE, rotated quad)
     const float *s_w = reinterpret_cast<const float *>(smem);
-    uint8_t *wsm = smem + SM::kWBytes + warp * SM::kWarpBytes;
+    float *s_rcp = reinterpret_cast<float *>(smem + SM::kWBytes);
+    const uint32_t wsm = smem_addr(smem) + SM::kWBytes + SM::kRcpBytes + warp * SM::kWarpBytes;  // this warp's ring
     const int64_t gw = int64_t(blockIdx.x) * kWarps + warp;
     int64_t start;
     int cnt;
@@ -547,6 +569,16 @@ __global__ void __launch_bounds__(32 * kWarps, 16 / kWarps) store_half_kernel(co
                            : static_cast<const void *>(static_cast<const int32_t *>(a.loc) + start));
         if constexpr (kRope) prefetch_l2(a.pos + start);
     }
+    if constexpr (L == Layout::FP4) {
+        // The correctly rounded reciprocal of every positive e4m3 scale (byte 0,
+        // a zero scale, gives zero codes and is never read).
+        for (int b = threadIdx.x; b < 128; b += 32 * kWarps) s_rcp[b] = __frcp_rn(e4m3x2_to_f32x2(b).x);
+        if constexpr (kWarps > 1) {
+            __syncthreads();
+        } else {
+            __syncwarp();
+        }
+    }
     pdl_wait();
 
     // With RoPE the first pair's rows go out before anything that could
@@ -561,7 +593,7 @@ __global__ void __launch_bounds__(32 * kWarps, 16 / kWarps) store_half_kernel(co
     const uint8_t *xw = a.x + start * a.row_stride_bytes;  // this warp's first row
     auto issue_rows = [&](int p) {
         if (p < npairs) {
-            uint8_t *slot = wsm + ring_in * SM::SLOT;
+            const uint32_t slot = wsm + ring_in * SM::SLOT;
             const uint8_t *r0 = xw + int64_t(2 * p) * a.row_stride_bytes;
 #pragma unroll
             for (int m = 0; m < NC; ++m) {
@@ -657,9 +689,9 @@ __global__ void __launch_bounds__(32 * kWarps, 16 / kWarps) store_half_kernel(co
         }
         cp_async_wait<kG * D - 1>();  // this lane's row copies of pair k have landed ...
         __syncwarp();                 // ... and so have the other lanes'
-        const uint8_t *slot_sm = wsm + ring_out * SM::SLOT;
+        const uint32_t slot_sm = wsm + ring_out * SM::SLOT;
         ring_out = (ring_out + 1) & (NS - 1);
-        const uint8_t *row = slot_sm + h * SM::XB;
+        const uint32_t row = slot_sm + h * SM::XB;
 
         // this lane's block (lanes 14 and 15 read the rotated blocks, unused with RoPE)
         float v[kBlock];
@@ -670,7 +702,7 @@ __global__ void __launch_bounds__(32 * kWarps, 16 / kWarps) store_half_kernel(co
         if constexpr (kRope) {
             const int blk = kRopeBlk0 + (bi >> 3);
             const int off = (4 * bi) & (kBlock - 1);  // first value of the quad inside its block
-            const uint8_t *qp = row + swz<SUBS>(blk, off / E) * 16 + (off % E) * (kBf16 ? 2 : 4);
+            const uint32_t qp = row + swz<SUBS>(blk, off / E) * 16 + (off % E) * (kBf16 ? 2 : 4);
             if constexpr (kBf16) {
                 const uint2 r = lds_u2(qp);
                 qv[0] = bf16_lo(r.x), qv[1] = bf16_hi(r.x), qv[2] = bf16_lo(r.y), qv[3] = bf16_hi(r.y);
@@ -747,12 +779,11 @@ __global__ void __launch_bounds__(32 * kWarps, 16 / kWarps) store_half_kernel(co
                     srow[bi] = uint8_t(sbyte);
                 }
             } else {
-                const uint32_t sbyte = fp4_scale_byte(__float_as_uint(am));
+                const uint32_t sbyte = fp4_scale_byte_fast(am);
                 if (bi < kOwn) {
-                    const float S = e4m3x2_to_f32x2(sbyte).x;
-                    const float inv = __frcp_rn(S);
+                    const float inv = s_rcp[sbyte];
                     uint32_t wd[4] = {0u, 0u, 0u, 0u};
-                    if (S != 0.0f) {
+                    if (sbyte != 0u) {
 #pragma unroll
                         for (int q = 0; q < 4; ++q) wd[q] = fp4_word(v + 8 * q, inv);
                     }
@@ -767,7 +798,7 @@ __global__ void __launch_bounds__(32 * kWarps, 16 / kWarps) store_half_kernel(co
         if constexpr (kRope) {
             cp_async_wait<2 * D>();  // (a refill of two groups was committed since)
             __syncwarp();
-            const uint8_t *cs = slot_sm + 2 * SM::XB + h * SM::CSB;
+            const uint32_t cs = slot_sm + 2 * SM::XB + h * SM::CSB;
             const uint2 cc = lds_u2(cs + 8 * bi), ss = lds_u2(cs + kRopeD * 2 + 8 * bi);
             const float cq[2] = {__uint_as_float(cc.x), __uint_as_float(cc.y)};
             const float sq[2] = {__uint_as_float(ss.x), __uint_as_float(ss.y)};
@@ -789,11 +820,10 @@ __global__ void __launch_bounds__(32 * kWarps, 16 / kWarps) store_half_kernel(co
                     *reinterpret_cast<uint32_t *>(crow + kRopeStart + 4 * bi) = v41_word(qv, v41_multiplier(sbq));
                     if ((bi & 7) == 0) srow[kRopeBlk0 + (bi >> 3)] = uint8_t(sbq);
                 } else {
-                    const uint32_t sbq = fp4_scale_byte(__float_as_uint(amq));
-                    const float S = e4m3x2_to_f32x2(sbq).x;
-                    const float inv = __frcp_rn(S);
+                    const uint32_t sbq = fp4_scale_byte_fast(amq);
+                    const float inv = s_rcp[sbq];
                     uint32_t w2 = 0;
-                    if (S != 0.0f) {
+                    if (sbq != 0u) {
                         const float2 y0 = fmul2(make_float2(qv[0], qv[1]), make_float2(inv, inv));
                         const float2 y1 = fmul2(make_float2(qv[2], qv[3]), make_float2(inv, inv));
                         w2 = cvt_e2m1x2(y0.x, y0.y) | (cvt_e2m1x2(y1.x, y1.y) << 8);
@@ -862,10 +892,10 @@ kvq_status launch_store(const StoreArgs &a, cudaStream_t stream) {
         }
         return launch_persistent<kern4, 4, 4 * wsm>(a, 1, 0, stream);
     } else if constexpr (L == Layout::V41) {
-        using SM = StoreSmem<B16, R, N>;
+        using SM = StoreSmem<L, B16, R, N>;
         return launch_persistent<store_half_kernel<L, PB, B16, L64, N, R, 1>, 1, SM::bytes(1)>(a, 2, 2, stream);
     } else {
-        using SM = StoreSmem<B16, R, N>;
+        using SM = StoreSmem<L, B16, R, N>;
         return launch_persistent<store_half_kernel<L, PB, B16, L64, N, R, 4>, 4, SM::bytes(4)>(a, 2, 0, stream);
     }
 }
