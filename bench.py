@@ -204,7 +204,7 @@ class StoreWorkload(Workload):
         payload = 528 if self.layout == 1 else 272
         per = row_bytes + 8 + payload + ((4 + 256) if self.flags & 1 else 0)
         self.bytes_total = self.bytes_dominant = bs * per
-        self.dominant = "store_warp_kernel" if self.layout == 1 else "store_pair_kernel"
+        self.dominant = "store_warp_kernel" if (self.layout == 1 and self.flags != 1) else "store_half_kernel"
         if sp.get("dequant"):   # the pool's pages back to bf16 after each store
             self.n_pages = self.pool_slots >> 6
             self.pt = torch.arange(self.n_pages, dtype=torch.int32, device=dev)

@@ -914,7 +914,7 @@ def test_bad_rows_in_a_large_batch(K, flags):
 
 @pytest.mark.parametrize("flags", [0, 1])
 def test_fp4_bad_rows_in_a_large_batch(K, flags):
-    """The FP4 pair kernel on 20000 tokens (several pairs per warp, so the
+    """The FP4 half-warp kernel on 20000 tokens (several pairs per warp, so the
     staggered first copy is in play) with out-of-range slots and positions:
     flagged, skipped, and every other row bit-exact to the oracle."""
     from compress_kv_write_gb300 import synth
