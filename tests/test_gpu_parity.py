@@ -199,6 +199,55 @@ def test_codec_e2m1_midpoints(K):
     assert (g[0] == rows_o[0]).all()
 
 
+def test_fp4_every_scale_byte(K):
+    """Every non-zero e4m3 block scale (bytes 1..126) through the FP4 store: a
+    block whose amax is 6 x the scale's value sets that scale, and its other
+    31 values sweep the e2m1 grid, its midpoints and their neighbours at that
+    scale (both signs).  The stored code and scale bytes, and the dequant,
+    must equal the oracle's, so every entry of the kernel's reciprocal table
+    and every scale its quotient can produce is exercised."""
+    codes = np.arange(1, 127, dtype=np.uint8)
+    S = O.e4m3_decode(codes)
+    amax = (S * 6).astype(np.float32)
+    assert (O.e4m3_encode((amax / np.float32(6)).astype(np.float32)) == codes).all()
+    grid = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6], np.float64)
+    mids = (grid[1:] + grid[:-1]) / 2
+    unit = np.concatenate([grid[:-1], mids, mids * (1 - 2.0**-20), mids * (1 + 2.0**-20)])  # 28 values
+    unit = np.concatenate([unit, [-0.25, -1.5, -3.0]])                                   # 31 values
+    rows = []
+    for i, s_ in enumerate(S):
+        blk = np.concatenate([[amax[i]], unit * s_]).astype(np.float32)
+        blk[1::2] *= -1 if i % 2 else 1
+        rows.append(blk)
+    nb = -(-len(rows) // 16) * 16
+    rows += [np.zeros(32, np.float32)] * (nb - len(rows))
+    x = np.stack(rows).reshape(-1, 512)
+    for dtype in ("f32", "bf16"):
+        xx = x if dtype == "f32" else O.bf16_bits(x).reshape(x.shape)
+        rows_o = _oracle_store_rows(O.FP4, 0, xx)
+        n = x.shape[0]
+        slots = -(-n // 64) * 64
+        pool = torch.zeros(slots * 288, dtype=torch.uint8, device=DEV)
+        xt = torch.from_numpy(x).to(DEV) if dtype == "f32" else \
+            torch.from_numpy(xx.view(np.int16)).view(torch.bfloat16).to(DEV)
+        err = _err(K)
+        K.kvq_store(K.V41_FP4, 6, 0, xt, torch.arange(n, device=DEV), pool, slots, err=err)
+        out = torch.empty((slots, 512), dtype=torch.bfloat16, device=DEV)
+        K.kvq_dequant(K.V41_FP4, 6, pool, slots // 64, torch.arange(slots // 64, dtype=torch.int32, device=DEV),
+                      out, err=err)
+        torch.cuda.synchronize()
+        assert err.item() == 0
+        g = gather_rows(np_u8(pool), O.FP4, 6, np.arange(n))
+        assert (g[1] == rows_o[1]).all(), dtype
+        assert (g[0] == rows_o[0]).all(), dtype
+        pool_o = np.zeros(slots * 288, np.uint8)
+        assert O.store(O.FP4, 6, 0, xx, np.arange(n), pool_o) == O.OK
+        rc, ws = O.dequant(O.FP4, 6, pool_o, np.arange(slots // 64, dtype=np.int32), slots)
+        assert rc == O.OK and (_bf16_np(out) == ws).all()
+        if dtype == "f32":  # every scale byte 1..126 appears
+            assert set(np.unique(g[1][:, :16])) >= set(range(1, 127))
+
+
 @pytest.mark.parametrize("layout", [1, 2])
 def test_codec_dequant_every_code_and_scale(K, layout):
     """Every (code, scale byte) pair through the paged dequant."""
