@@ -248,14 +248,8 @@ __device__ __forceinline__ uint32_t smem_addr(const void *p) {
 }
 
 // Per-thread async copies global -> shared (LSU path, no register cost),
-// grouped per thread with commit / wait_group.
-__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async8(void *dst, const void *src) {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
-}
-// The same with a shared-window address (32 bits, from smem_addr).
+// grouped per thread with commit / wait_group; dst is a shared-window
+// address (32 bits, from smem_addr).
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
@@ -292,12 +286,7 @@ __device__ __forceinline__ void prefetch_l1(const void *p) {
     asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
 }
 
-__device__ __forceinline__ uint2 lds_u2(const void *p) {
-    uint2 r;
-    asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "r"(smem_addr(p)));
-    return r;
-}
-
+// Shared-memory loads from a shared-window address.
 __device__ __forceinline__ uint2 lds_u2(uint32_t a) {
     uint2 r;
     asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "r"(a));
@@ -307,14 +296,6 @@ __device__ __forceinline__ uint2 lds_u2(uint32_t a) {
 __device__ __forceinline__ uint4 lds_u4(uint32_t a) {
     uint4 r;
     asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "r"(a));
-    return r;
-}
-
-__device__ __forceinline__ uint4 lds_u4(const void *p) {
-    uint4 r;
-    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-                 : "r"(smem_addr(p)));
     return r;
 }
 

@@ -134,53 +134,32 @@ __device__ __forceinline__ void block_amax(float (&v)[K][E], float (&am)[K]) {
     }
 }
 
-// Quantise chunks K0 .. K1-1 with their block absmax into the token's code
-// row and scale row.  The lane that leads a quant block writes its scale byte.
+// Quantise chunks K0 .. K1-1 with their block absmax into the token's V41
+// code row and scale row.  The lane that leads a quant block writes its
+// scale byte.
 template <Layout L, int E, int K, int K0, int K1>
 __device__ __forceinline__ void quant_store(float (&v)[K][E], const float (&am)[K], uint8_t *crow, uint8_t *srow,
                                             int lane) {
+    static_assert(L == Layout::V41, "the one-warp-per-token mapping serves V41 only");
     constexpr int LPB = kBlock / E;
 #pragma unroll
     for (int k = K0; k < K1; ++k) {
         const int c = k * 32 + lane;  // chunk index in the row
-        uint32_t sbyte;
-        if constexpr (L == Layout::V41) {
-            sbyte = v41_scale_byte(__float_as_uint(am[k]));
-            const float mult = v41_multiplier(sbyte);
-            uint32_t wds[E / 4];
+        const uint32_t sbyte = v41_scale_byte(__float_as_uint(am[k]));
+        const float mult = v41_multiplier(sbyte);
+        uint32_t wds[E / 4];
 #pragma unroll
-            for (int q = 0; q < E / 4; ++q) {
-                const float2 a = fmul2(make_float2(v[k][4 * q], v[k][4 * q + 1]), make_float2(mult, mult));
-                const float2 b = fmul2(make_float2(v[k][4 * q + 2], v[k][4 * q + 3]), make_float2(mult, mult));
-                wds[q] = cvt_e4m3x2(a.x, a.y) | (cvt_e4m3x2(b.x, b.y) << 16);
-            }
-            if constexpr (E == 8) {
-                *reinterpret_cast<uint2 *>(crow + c * 8) = make_uint2(wds[0], wds[1]);
-            } else {
-                *reinterpret_cast<uint32_t *>(crow + c * 4) = wds[0];
-            }
+        for (int q = 0; q < E / 4; ++q) {
+            const float2 a = fmul2(make_float2(v[k][4 * q], v[k][4 * q + 1]), make_float2(mult, mult));
+            const float2 b = fmul2(make_float2(v[k][4 * q + 2], v[k][4 * q + 3]), make_float2(mult, mult));
+            wds[q] = cvt_e4m3x2(a.x, a.y) | (cvt_e4m3x2(b.x, b.y) << 16);
+        }
+        if constexpr (E == 8) {
+            *reinterpret_cast<uint2 *>(crow + c * 8) = make_uint2(wds[0], wds[1]);
         } else {
-            sbyte = fp4_scale_byte(__float_as_uint(am[k]));
-            const float S = e4m3x2_to_f32x2(sbyte).x;
-            const float inv = __frcp_rn(S);
-            uint32_t word = 0;
-            if (S != 0.0f) {
-#pragma unroll
-                for (int q = 0; q < E / 2; ++q) {
-                    const float2 a = fmul2(make_float2(v[k][2 * q], v[k][2 * q + 1]), make_float2(inv, inv));
-                    word |= cvt_e2m1x2(a.x, a.y) << (8 * q);
-                }
-            }
-            if constexpr (E == 8) {
-                *reinterpret_cast<uint32_t *>(crow + c * 4) = word;
-            } else {
-                *reinterpret_cast<uint16_t *>(crow + c * 2) = uint16_t(word);
-            }
+            *reinterpret_cast<uint32_t *>(crow + c * 4) = wds[0];
         }
         if (lane % LPB == 0) srow[c / LPB] = uint8_t(sbyte);
-    }
-    if constexpr (LayoutTraits<L>::kScaleBytes == 32 && K1 == K) {
-        if (lane == 0) st_u4(srow + 16, make_uint4(0u, 0u, 0u, 0u));
     }
 }
 
