@@ -11,12 +11,17 @@ namespace {
 // Decode-time compressor: one new row per request per call, the group's
 // softmax carried between calls as per-dim online state (running max m,
 // sum of exp(s - m) and sum of exp(s - m) * v), 3 x 512 fp32 per request.
-// One warp per request: lane l owns the float4 columns l, l+32, l+64, l+96,
-// so every warp access is one contiguous 512-byte span, a quant block is 8
-// adjacent lanes, and the request's count is read and rewritten by the same
-// warp (ordered by __syncwarp).
+// One CTA of four warps per request: warp w owns the dims 128 w .. 128 w +
+// 127, lane l of it the float4 column 32 w + l, so every warp access is one
+// contiguous 512-byte span and a quant block is 8 adjacent lanes.  Four
+// warps per request rather than one make each request's dependent chain of
+// loads, exponentials, divisions, shuffles and conversions a quarter as long
+// (the whole launch at small batches) and keep four times as many rows in
+// flight per resident request at large ones.  The count is read by every
+// thread of the CTA and rewritten by thread 0 after a barrier.
 
-constexpr int kDecWarps = 4;
+constexpr int kDecWarps = 4;  // warps per CTA: one request
+static_assert(kDecWarps * 32 * 4 == kD, "one float4 column per thread");
 
 struct DecodeArgs {
     const float *values;
@@ -34,24 +39,22 @@ struct DecodeArgs {
     int64_t pool_slots;
     int32_t *err;
     int warm;  // prefetch each request's row and state into L2 before the PDL wait
-    int spec;  // small batch: pull the state into L1 while the row count is read
 };
 
 template <Layout L, int PageBits, int R, bool kRope>
 __global__ void __launch_bounds__(kDecWarps * 32) compress_decode_kernel(const DecodeArgs a) {
     using PK = PagedKV<L, PageBits>;
     using T = LayoutTraits<L>;
-    constexpr int K = kD / 4 / 32;  // float4 columns per lane
-    const int lane = threadIdx.x & 31;
-    const int64_t i = int64_t(blockIdx.x) * kDecWarps + (threadIdx.x >> 5);
-    if (i >= a.n) return;  // whole warps; no block barrier follows
+    const int t = threadIdx.x;   // float4 column: dims 4t .. 4t+3, quant block t / 8
+    const int lane = t & 31;
+    const int64_t i = blockIdx.x;  // the request (the grid is exactly n CTAs)
     // While the upstream grid drains: L2 hints for this request's new row and
     // its state (hints only; every load below comes after the wait).
     if (a.warm) {
         const int64_t rh = a.req ? -1 : i;  // the state row is known only without an index array
-        if (lane == 0) prefetch_l2_bulk(a.values + i * kD, kD * 4);
-        if (lane == 1) prefetch_l2_bulk(a.scores + i * kD, kD * 4);
-        if (lane == 2 && rh >= 0 && rh < a.n_state) prefetch_l2_bulk(a.state + rh * (3 * kD), 3 * kD * 4);
+        if (t == 0) prefetch_l2_bulk(a.values + i * kD, kD * 4);
+        if (t == 32) prefetch_l2_bulk(a.scores + i * kD, kD * 4);
+        if (t == 64 && rh >= 0 && rh < a.n_state) prefetch_l2_bulk(a.state + rh * (3 * kD), 3 * kD * 4);
     }
     pdl_wait();
 
@@ -60,150 +63,115 @@ __global__ void __launch_bounds__(kDecWarps * 32) compress_decode_kernel(const D
     // where every row completes a group, its cos/sin values).  Only the state
     // waits for the count.
     const int64_t ri = a.req ? int64_t(__ldg(a.req + i)) : i;
-    float4 vr[K], sr[K];
-#pragma unroll
-    for (int k = 0; k < K; ++k) {
-        vr[k] = ld_f4(a.values + i * kD + 4 * (k * 32 + lane));
-        sr[k] = ld_f4(a.scores + i * kD + 4 * (k * 32 + lane));
-    }
+    const float4 v = ld_f4(a.values + i * kD + 4 * t);
+    const float4 sc = ld_f4(a.scores + i * kD + 4 * t);
     const int64_t slot = __ldg(a.loc + i);
     const int32_t pos = kRope ? __ldg(a.group_pos + i) : 0;
     const bool pos_ok = !kRope || (pos >= 0 && int64_t(pos) < a.cs_rows);
-    const int rope_col = 4 * ((K - 1) * 32 + lane);  // rope dims sit in the last column set
+    const bool rope_col = kRope && 4 * t >= kRopeStart;  // rotated dims of this column
     float2 cs_c = make_float2(1.f, 1.f), cs_s = make_float2(0.f, 0.f);
     auto load_cs = [&]() {
-        if (kRope && pos_ok && rope_col >= kRopeStart) {
-            const int i0 = (rope_col - kRopeStart) / 2;
+        if (rope_col && pos_ok) {
+            const int i0 = (4 * t - kRopeStart) / 2;
             const float *cs = a.cs + int64_t(pos) * kRopeD;
             cs_c = __ldg(reinterpret_cast<const float2 *>(cs + i0));
             cs_s = __ldg(reinterpret_cast<const float2 *>(cs + kRopeD / 2 + i0));
         }
     };
     if constexpr (R == 1) load_cs();
-    if constexpr (R > 1) {
-        // The state row's address does not depend on the count: in a latency
-        // case fetch its 48 lines now, so the loads below hit L1.
-        if (a.spec && ri >= 0 && ri < a.n_state) {
-            const uint8_t *sb = reinterpret_cast<const uint8_t *>(a.state + ri * (3 * kD));
-            prefetch_l1(sb + lane * 128);
-            if (lane < 3 * kD * 4 / 128 - 32) prefetch_l1(sb + (32 + lane) * 128);
-        }
-    }
     pdl_trigger();  // the next launch may start its prologue; its wait still covers this grid
     const int32_t c = (ri >= 0 && ri < a.n_state) ? a.count[ri] : -1;
-    __syncwarp();  // every lane has read the count before lane 0 rewrites it
+    __syncthreads();  // every thread has read the count before thread 0 rewrites it
     if (c < 0 || c >= R) {
-        if (lane == 0) raise_err(a.err, KVQ_DEVERR_STATE);
+        if (t == 0) raise_err(a.err, KVQ_DEVERR_STATE);
         return;
     }
     if constexpr (R > 1) {
         if (c == R - 1) load_cs();
     }
-    float4 m[K], l[K], acc[K];
-    float *st = a.state + ri * (3 * kD);
+    float *st = a.state + ri * (3 * kD) + 4 * t;
+    float4 m = sc, l = make_float4(1.f, 1.f, 1.f, 1.f), acc = v;
+    if (c > 0) {
+        const float4 m0 = *reinterpret_cast<const float4 *>(st);
+        const float4 l0 = *reinterpret_cast<const float4 *>(st + kD);
+        const float4 a0 = *reinterpret_cast<const float4 *>(st + 2 * kD);
 #pragma unroll
-    for (int k = 0; k < K; ++k) {
-        const int col = 4 * (k * 32 + lane);
-        const float4 v = vr[k];
-        const float4 sc = sr[k];
-        m[k] = sc;
-        l[k] = make_float4(1.f, 1.f, 1.f, 1.f);
-        acc[k] = v;
-        if (c > 0) {
-            const float4 m0 = *reinterpret_cast<const float4 *>(st + col);
-            const float4 l0 = *reinterpret_cast<const float4 *>(st + kD + col);
-            const float4 a0 = *reinterpret_cast<const float4 *>(st + 2 * kD + col);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float mo = (&m0.x)[e], so = (&sc.x)[e];
-                const float mn = fmaxf(mo, so);
-                const float al = ex2_approx((mo - mn) * kLog2e);
-                const float p = ex2_approx((so - mn) * kLog2e);
-                (&m[k].x)[e] = mn;
-                (&l[k].x)[e] = fmaf((&l0.x)[e], al, p);
-                (&acc[k].x)[e] = fmaf(p, (&v.x)[e], (&a0.x)[e] * al);
-            }
+        for (int e = 0; e < 4; ++e) {
+            const float mo = (&m0.x)[e], so = (&sc.x)[e];
+            const float mn = fmaxf(mo, so);
+            const float al = ex2_approx((mo - mn) * kLog2e);
+            const float p = ex2_approx((so - mn) * kLog2e);
+            (&m.x)[e] = mn;
+            (&l.x)[e] = fmaf((&l0.x)[e], al, p);
+            (&acc.x)[e] = fmaf(p, (&v.x)[e], (&a0.x)[e] * al);
         }
     }
     if (c + 1 < R) {  // the group is still open: keep the state
-#pragma unroll
-        for (int k = 0; k < K; ++k) {
-            const int col = 4 * (k * 32 + lane);
-            *reinterpret_cast<float4 *>(st + col) = m[k];
-            *reinterpret_cast<float4 *>(st + kD + col) = l[k];
-            *reinterpret_cast<float4 *>(st + 2 * kD + col) = acc[k];
-        }
-        if (lane == 0) a.count[ri] = c + 1;
+        *reinterpret_cast<float4 *>(st) = m;
+        *reinterpret_cast<float4 *>(st + kD) = l;
+        *reinterpret_cast<float4 *>(st + 2 * kD) = acc;
+        if (t == 0) a.count[ri] = c + 1;
         return;
     }
     // the group is complete: pool, rotate, round, quantise, store; restart
-    if (R > 1 && lane == 0) a.count[ri] = 0;  // ratio 1: the count is 0 already
-    float y[K][4];
+    if (R > 1 && t == 0) a.count[ri] = 0;  // ratio 1: the count is 0 already
+    float y[4];
 #pragma unroll
-    for (int k = 0; k < K; ++k)
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-            y[k][e] = R == 1 ? (&acc[k].x)[e] : __fdiv_rn((&acc[k].x)[e], (&l[k].x)[e]);  // ratio 1: l = 1
-    if (kRope && pos_ok && rope_col >= kRopeStart) {
+    for (int e = 0; e < 4; ++e) y[e] = R == 1 ? (&acc.x)[e] : __fdiv_rn((&acc.x)[e], (&l.x)[e]);  // ratio 1: l = 1
+    if (rope_col && pos_ok) {
         const float c2[2] = {cs_c.x, cs_c.y}, s2[2] = {cs_s.x, cs_s.y};
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
-            const float x0 = y[K - 1][2 * q], x1 = y[K - 1][2 * q + 1];
-            y[K - 1][2 * q] = __fsub_rn(__fmul_rn(x0, c2[q]), __fmul_rn(x1, s2[q]));
-            y[K - 1][2 * q + 1] = __fadd_rn(__fmul_rn(x0, s2[q]), __fmul_rn(x1, c2[q]));
+            const float x0 = y[2 * q], x1 = y[2 * q + 1];
+            y[2 * q] = __fsub_rn(__fmul_rn(x0, c2[q]), __fmul_rn(x1, s2[q]));
+            y[2 * q + 1] = __fadd_rn(__fmul_rn(x0, s2[q]), __fmul_rn(x1, c2[q]));
         }
     }
     if (!pos_ok || slot < 0 || slot >= a.pool_slots) {
-        if (lane == 0) raise_err(a.err, pos_ok ? KVQ_DEVERR_SLOT : KVQ_DEVERR_POS);
+        if (t == 0) raise_err(a.err, pos_ok ? KVQ_DEVERR_SLOT : KVQ_DEVERR_POS);
         return;
     }
     uint8_t *crow = PK::code_row(a.pool, slot);
     uint8_t *srow = PK::scale_row(a.pool, slot);
 #pragma unroll
-    for (int k = 0; k < K; ++k) {
+    for (int e = 0; e < 4; ++e) y[e] = round_bf16(y[e]);
+    uint32_t am = max(max(abs_bits(y[0]), abs_bits(y[1])), max(abs_bits(y[2]), abs_bits(y[3])));
 #pragma unroll
-        for (int e = 0; e < 4; ++e) y[k][e] = round_bf16(y[k][e]);
-        uint32_t am = max(max(abs_bits(y[k][0]), abs_bits(y[k][1])), max(abs_bits(y[k][2]), abs_bits(y[k][3])));
-#pragma unroll
-        for (int off = 1; off < 8; off <<= 1) am = max(am, __shfl_xor_sync(0xffffffffu, am, off));
-        const int colq = k * 32 + lane;  // float4 column: dims 4colq .. 4colq+3, block colq / 8
-        uint32_t sbyte;
-        if constexpr (L == Layout::V41) {
-            sbyte = v41_scale_byte(am);
-            const float mult = v41_multiplier(sbyte);
-            const uint32_t lo = cvt_e4m3x2(__fmul_rn(y[k][0], mult), __fmul_rn(y[k][1], mult));
-            const uint32_t hi = cvt_e4m3x2(__fmul_rn(y[k][2], mult), __fmul_rn(y[k][3], mult));
-            *reinterpret_cast<uint32_t *>(crow + 4 * colq) = lo | (hi << 16);
-        } else {
-            sbyte = fp4_scale_byte(am);
-            const float S = e4m3x2_to_f32x2(sbyte).x;
-            const float inv = __frcp_rn(S);
-            uint32_t word = 0;
-            if (S != 0.0f)
-                word = cvt_e2m1x2(__fmul_rn(y[k][0], inv), __fmul_rn(y[k][1], inv)) |
-                       (cvt_e2m1x2(__fmul_rn(y[k][2], inv), __fmul_rn(y[k][3], inv)) << 8);
-            *reinterpret_cast<uint16_t *>(crow + 2 * colq) = uint16_t(word);
-        }
-        if ((lane & 7) == 0) srow[colq >> 3] = uint8_t(sbyte);
+    for (int off = 1; off < 8; off <<= 1) am = max(am, __shfl_xor_sync(0xffffffffu, am, off));
+    uint32_t sbyte;
+    if constexpr (L == Layout::V41) {
+        sbyte = v41_scale_byte(am);
+        const float mult = v41_multiplier(sbyte);
+        const uint32_t lo = cvt_e4m3x2(__fmul_rn(y[0], mult), __fmul_rn(y[1], mult));
+        const uint32_t hi = cvt_e4m3x2(__fmul_rn(y[2], mult), __fmul_rn(y[3], mult));
+        *reinterpret_cast<uint32_t *>(crow + 4 * t) = lo | (hi << 16);
+    } else {
+        sbyte = fp4_scale_byte(am);
+        const float S = e4m3x2_to_f32x2(sbyte).x;
+        const float inv = __frcp_rn(S);
+        uint32_t word = 0;
+        if (S != 0.0f)
+            word = cvt_e2m1x2(__fmul_rn(y[0], inv), __fmul_rn(y[1], inv)) |
+                   (cvt_e2m1x2(__fmul_rn(y[2], inv), __fmul_rn(y[3], inv)) << 8);
+        *reinterpret_cast<uint16_t *>(crow + 2 * t) = uint16_t(word);
     }
+    if ((lane & 7) == 0) srow[t >> 3] = uint8_t(sbyte);
     if constexpr (T::kScaleBytes == 32) {
-        if (lane == 0) st_u4(srow + 16, make_uint4(0u, 0u, 0u, 0u));
+        if (t == 0) st_u4(srow + 16, make_uint4(0u, 0u, 0u, 0u));
     }
 }
 
 template <Layout L, int PB, int R, bool RP>
 kvq_status launch_compress_decode(DecodeArgs a, cudaStream_t stream) {
-    const int64_t blocks = (a.n + kDecWarps - 1) / kDecWarps;
-    if (blocks > 0x7FFFFFFF) return KVQ_ERR_INVALID_ARG;
+    constexpr auto kern = compress_decode_kernel<L, PB, R, RP>;
+    if (a.n > 0x7FFFFFFF) return KVQ_ERR_INVALID_ARG;
     int64_t wave = 0;
-    const kvq_status st = resident_grid<compress_decode_kernel<L, PB, R, RP>, kDecWarps * 32>(0, &wave);
+    const kvq_status st = resident_grid<kern, kDecWarps * 32>(0, &wave);
     if (st != KVQ_OK) return st;
     // Beyond one wave the hints would only duplicate the loads of CTAs that
     // start after the upstream grid has finished.
-    a.warm = blocks <= wave;
-    a.spec = a.n < 4096;
-    return launch_pdl(compress_decode_kernel<L, PB, R, RP>, dim3(unsigned(blocks)), dim3(kDecWarps * 32),
-                      stream, a);
+    a.warm = a.n <= wave;
+    return launch_pdl(kern, dim3(unsigned(a.n)), dim3(kDecWarps * 32), stream, a);
 }
 
 }  // namespace
