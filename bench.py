@@ -172,6 +172,15 @@ def _rotation(per_set_bytes, cap=64):
     return max(1, min(cap, math.ceil(2.5 * L2_BYTES / max(1, per_set_bytes))))
 
 
+def store_kernel_name(layout, flags, bs):
+    """The store kernel a batch of bs tokens runs on (layout 1 = V41): the
+    library takes one CTA per token up to 1024 tokens (512 for the plain V41
+    store), its persistent kernels beyond."""
+    if bs <= (512 if (layout == 1 and flags == 0) else 1024):
+        return "store_token_kernel"
+    return "store_warp_kernel" if (layout == 1 and flags != 1) else "store_half_kernel"
+
+
 class StoreWorkload(Workload):
     """bs rows -> paged pool: store, store + RoPE, fused K RMSNorm + RoPE."""
 
@@ -204,7 +213,7 @@ class StoreWorkload(Workload):
         payload = 528 if self.layout == 1 else 272
         per = row_bytes + 8 + payload + ((4 + 256) if self.flags & 1 else 0)
         self.bytes_total = self.bytes_dominant = bs * per
-        self.dominant = "store_warp_kernel" if (self.layout == 1 and self.flags != 1) else "store_half_kernel"
+        self.dominant = store_kernel_name(self.layout, self.flags, bs)
         if sp.get("dequant"):   # the pool's pages back to bf16 after each store
             self.n_pages = self.pool_slots >> 6
             self.pt = torch.arange(self.n_pages, dtype=torch.int32, device=dev)
@@ -570,7 +579,7 @@ class LayersWorkload(Workload):
         per_store = self.bs * B_STORE_ROPE
         self.bytes_dominant = per_store
         self.bytes_total = self.L * per_store + self.bs * B_TRANSLATE
-        self.dominant = "store_warp_kernel"
+        self.dominant = store_kernel_name(1, self.flags, self.bs)
         self.config["l2"] = (f"rotating {self.R} step input sets ({self.R * per_set / 2**20:.0f} MB) "
                              f"over {self.L} pools of {self.swa_slots * 528 / 2**20:.0f} MB")
 
@@ -717,8 +726,9 @@ def measured_hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-KERNEL_SOURCES = {"store": "kvq_store.cu", "dequant": "kvq_dequant.cu", "compress": "kvq_compress.cu",
-                  "layers": "kvq_store.cu", "select": "kvq_dequant.cu", "decode": "kvq_decode.cu"}
+_STORE_SOURCES = ("kvq_store.cu", "kvq_store_small.cu", "kvq_store.cuh")
+KERNEL_SOURCES = {"store": _STORE_SOURCES, "dequant": ("kvq_dequant.cu",), "compress": ("kvq_compress.cu",),
+                  "layers": _STORE_SOURCES, "select": ("kvq_dequant.cu",), "decode": ("kvq_decode.cu",)}
 
 
 def traffic_from_profiles(workload):
@@ -753,7 +763,7 @@ def kernel_source_sha(workload):
     import hashlib
     h = hashlib.sha256()
     d = os.path.join(ROOT, "compress_kv_write_gb300", "csrc")
-    files = [KERNEL_SOURCES[SPECS[workload]["kind"]], "kvq_device.cuh", "kvq_launch.cuh"]
+    files = [*KERNEL_SOURCES[SPECS[workload]["kind"]], "kvq_device.cuh", "kvq_launch.cuh"]
     for fn in files:
         with open(os.path.join(d, fn), encoding="utf-8") as f:
             h.update(fn.encode())

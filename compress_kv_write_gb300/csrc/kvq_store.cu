@@ -31,31 +31,10 @@
 // L2.  Slot indices and positions of 32 tokens sit one per lane, validated
 // once, and are fetched with a shuffle.  Math is fp32; the products of the
 // RMSNorm and of the rotation are rounded one by one, as in the definition.
-#include "kvq_launch.cuh"
+#include "kvq_store.cuh"
 
 namespace kvq {
 namespace {
-
-struct StoreArgs {
-    const uint8_t *x;
-    int64_t n;
-    int64_t row_stride_bytes;
-    const void *loc;
-    const float *w;
-    float eps;
-    const float *cs;
-    int64_t cs_rows;
-    const int32_t *pos;
-    uint8_t *pool;
-    int64_t pool_slots;
-    int32_t *err;
-    // token ranges (set by partition()): per_warp tokens per warp, one more
-    // for the first extra + skew warps, one fewer for the last skew warps
-    int64_t per_warp;
-    int64_t extra;
-    int64_t skew;
-    int64_t warps;
-};
 
 // Token range [start, start + cnt) of warp gw (see StoreArgs).
 __device__ __forceinline__ void token_range(const StoreArgs &a, int64_t gw, int64_t &start, int &cnt) {
@@ -934,6 +913,8 @@ extern "C" kvq_status kvq_store(kvq_layout layout, int page_bits, unsigned flags
     a.pool_slots = pool_slots;
     a.err = err;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (n <= store_small_max(layout, norm, rope))
+        return launch_store_small(layout, page_bits, x_dtype == KVQ_BF16, loc_dtype == KVQ_I64, norm, rope, a, s);
     return with_layout(layout, [&](auto Lc) {
         return with_page_bits(page_bits, [&](auto PBc) {
             return with_bool(x_dtype == KVQ_BF16, [&](auto B16) {

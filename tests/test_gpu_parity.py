@@ -85,14 +85,16 @@ def test_fp32_store_and_dequant_64_tokens(K):
 @pytest.mark.parametrize("loc64", [False, True])
 @pytest.mark.parametrize("flags", [0, 1, 2, 3])
 def test_store_instances_ragged(K, page_bits, layout, dtype, loc64, flags):
-    """Every store instance on ragged batches (1, 37, 301 rows): the plain and
-    RoPE paths bit-exact over the whole pool; the norm paths under the
-    tolerance rule, the three batches pooled into one comparison."""
+    """Every store instance on ragged batches: 1, 37 and 301 rows (batches of
+    up to 1024 tokens take one CTA per token) and 1537 rows (the persistent
+    kernels).  The plain and RoPE paths bit-exact over the whole pool; the
+    norm paths under the tolerance rule, the four batches pooled into one
+    comparison."""
     from compress_kv_write_gb300 import synth
-    slots = 1024
+    slots = 2048
     rng_seed = page_bits * 1000 + layout * 100 + flags * 10 + int(loc64)
     acc = [[], [], [], [], []]
-    for n in (1, 37, 301):
+    for n in (1, 37, 301, 1537):
         x = synth.store_rows_bf16(n, "cpu", rng_seed + n)
         if dtype == "f32":
             x = x.float() * 1.25          # not bf16-representable in general
@@ -130,25 +132,34 @@ def test_store_instances_ragged(K, page_bits, layout, dtype, loc64, flags):
 
 # --------------------------------------------------------------------------- codecs
 
+def _both_paths(x):
+    """x (up to 1024 rows: one CTA per token) and x tiled past 1024 rows (the
+    persistent kernels), so that a codec pin covers both store mappings."""
+    return [x, np.tile(x, (-(-1025 // x.shape[0]), 1))]
+
+
 def test_codec_every_bf16_pattern(K):
-    """All finite bf16 bit patterns through the plain store, both layouts."""
+    """All finite bf16 bit patterns through the plain store, both layouts,
+    both store mappings."""
     bits = np.arange(65536, dtype=np.uint32)
     finite = ((bits >> 7) & 0xFF) != 0xFF
     pat = bits[finite].astype(np.uint16)
     rng = np.random.default_rng(0)
     pat = pat[rng.permutation(pat.size)]
     pad = (-pat.size) % 512
-    pat = np.concatenate([pat, np.zeros(pad, np.uint16)]).reshape(-1, 512)
-    n = pat.shape[0]
-    x = torch.from_numpy(pat.view(np.int16)).view(torch.bfloat16).to(DEV)
-    for layout in (1, 2):
-        rows_o = _oracle_store_rows(layout, 0, pat)
-        pool = torch.zeros(256 * O.bytes_per_token(layout), dtype=torch.uint8, device=DEV)
-        loc = torch.arange(n, dtype=torch.int32, device=DEV)
-        K.kvq_store(layout, 6, 0, x, loc, pool, 256)
-        torch.cuda.synchronize()
-        g = gather_rows(np_u8(pool), layout, 6, np.arange(n))
-        assert (g[0] == rows_o[0]).all() and (g[1] == rows_o[1]).all()
+    pat1 = np.concatenate([pat, np.zeros(pad, np.uint16)]).reshape(-1, 512)
+    for pat in _both_paths(pat1):
+        n = pat.shape[0]
+        slots = -(-n // 64) * 64
+        x = torch.from_numpy(pat.view(np.int16)).view(torch.bfloat16).to(DEV)
+        for layout in (1, 2):
+            rows_o = _oracle_store_rows(layout, 0, pat)
+            pool = torch.zeros(slots * O.bytes_per_token(layout), dtype=torch.uint8, device=DEV)
+            loc = torch.arange(n, dtype=torch.int32, device=DEV)
+            K.kvq_store(layout, 6, 0, x, loc, pool, slots)
+            torch.cuda.synchronize()
+            g = gather_rows(np_u8(pool), layout, 6, np.arange(n))
+            assert (g[0] == rows_o[0]).all() and (g[1] == rows_o[1]).all(), (n, layout)
 
 
 def _midpoint_rows(anchor, grid):
@@ -172,15 +183,16 @@ def test_codec_e4m3_midpoints(K):
     grid = np.unique(O.e4m3_decode(codes))
     x = _midpoint_rows(448.0, grid)          # byte 127: multiplier 1
     x = np.concatenate([x, _midpoint_rows(511.0, np.array([448.0, 460.0, 464.0, 480.0, 500.0]))])
-    rows_o = _oracle_store_rows(O.V41, 0, x)
-    n = x.shape[0]
-    pool = torch.zeros(-(-n // 64) * 64 * 528, dtype=torch.uint8, device=DEV)
-    K.kvq_store(K.V41, 6, 0, torch.from_numpy(x).to(DEV), torch.arange(n, device=DEV), pool,
-                -(-n // 64) * 64)
-    torch.cuda.synchronize()
-    g = gather_rows(np_u8(pool), O.V41, 6, np.arange(n))
-    assert (g[1] == rows_o[1]).all()
-    assert (g[0] == rows_o[0]).all(), np.argwhere(g[0] != rows_o[0])[:5]
+    for x in _both_paths(x):
+        rows_o = _oracle_store_rows(O.V41, 0, x)
+        n = x.shape[0]
+        pool = torch.zeros(-(-n // 64) * 64 * 528, dtype=torch.uint8, device=DEV)
+        K.kvq_store(K.V41, 6, 0, torch.from_numpy(x).to(DEV), torch.arange(n, device=DEV), pool,
+                    -(-n // 64) * 64)
+        torch.cuda.synchronize()
+        g = gather_rows(np_u8(pool), O.V41, 6, np.arange(n))
+        assert (g[1] == rows_o[1]).all(), n
+        assert (g[0] == rows_o[0]).all(), (n, np.argwhere(g[0] != rows_o[0])[:5])
 
 
 def test_codec_e2m1_midpoints(K):
@@ -188,15 +200,16 @@ def test_codec_e2m1_midpoints(K):
     x = _midpoint_rows(6.0, grid)            # scale 1.0
     x = np.concatenate([x, _midpoint_rows(6.0, np.array([5.9, 6.0, 6.2, 7.0, 100.0]))])
     x = np.clip(x, -6, 6)                    # keep the block amax at 6
-    rows_o = _oracle_store_rows(O.FP4, 0, x)
-    n = x.shape[0]
-    slots = -(-n // 64) * 64
-    pool = torch.zeros(slots * 288, dtype=torch.uint8, device=DEV)
-    K.kvq_store(K.V41_FP4, 6, 0, torch.from_numpy(x).to(DEV), torch.arange(n, device=DEV), pool, slots)
-    torch.cuda.synchronize()
-    g = gather_rows(np_u8(pool), O.FP4, 6, np.arange(n))
-    assert (g[1] == rows_o[1]).all()
-    assert (g[0] == rows_o[0]).all()
+    for x in _both_paths(x):
+        rows_o = _oracle_store_rows(O.FP4, 0, x)
+        n = x.shape[0]
+        slots = -(-n // 64) * 64
+        pool = torch.zeros(slots * 288, dtype=torch.uint8, device=DEV)
+        K.kvq_store(K.V41_FP4, 6, 0, torch.from_numpy(x).to(DEV), torch.arange(n, device=DEV), pool, slots)
+        torch.cuda.synchronize()
+        g = gather_rows(np_u8(pool), O.FP4, 6, np.arange(n))
+        assert (g[1] == rows_o[1]).all(), n
+        assert (g[0] == rows_o[0]).all(), n
 
 
 def test_fp4_every_scale_byte(K):
@@ -205,7 +218,9 @@ def test_fp4_every_scale_byte(K):
     31 values sweep the e2m1 grid, its midpoints and their neighbours at that
     scale (both signs).  The stored code and scale bytes, and the dequant,
     must equal the oracle's, so every entry of the kernel's reciprocal table
-    and every scale its quotient can produce is exercised."""
+    and every scale its quotient can produce is exercised.  The 8 rows run
+    alone (one CTA per token) and tiled to 1032 rows (the persistent kernel
+    with its reciprocal table)."""
     codes = np.arange(1, 127, dtype=np.uint8)
     S = O.e4m3_decode(codes)
     amax = (S * 6).astype(np.float32)
@@ -221,8 +236,9 @@ def test_fp4_every_scale_byte(K):
         rows.append(blk)
     nb = -(-len(rows) // 16) * 16
     rows += [np.zeros(32, np.float32)] * (nb - len(rows))
-    x = np.stack(rows).reshape(-1, 512)
-    for dtype in ("f32", "bf16"):
+    x1 = np.stack(rows).reshape(-1, 512)
+    for dtype, reps in (("f32", 1), ("bf16", 1), ("f32", 129), ("bf16", 129)):
+        x = np.tile(x1, (reps, 1))
         xx = x if dtype == "f32" else O.bf16_bits(x).reshape(x.shape)
         rows_o = _oracle_store_rows(O.FP4, 0, xx)
         n = x.shape[0]
@@ -293,13 +309,14 @@ def sweep_inputs():
 def test_store_batch_sweep(K, sweep_inputs, flags):
     """bf16 rows with outliers, pool of 2^20 slots: store, store + RoPE and
     fused K RMSNorm + RoPE at every batch size of the sweep (1, 8, 64, 512,
-    16384), each into a fresh pool.  Plain and RoPE stores are bit-exact;
-    the fused norm path follows the tolerance rule with the five batches
-    pooled into one comparison."""
+    16384) and on both sides of the one-CTA-per-token limit (1024, 1025),
+    each into a fresh pool.  Plain and RoPE stores are bit-exact; the fused
+    norm path follows the tolerance rule with the batches pooled into one
+    comparison."""
     x_all, loc_all, pos_all, cs, w = sweep_inputs
     cs_np, w_np = cs.cpu().numpy(), w.cpu().numpy()
     acc = [[], [], [], [], []]
-    for bs in (1, 8, 64, 512, 16384):
+    for bs in (1, 8, 64, 512, 1024, 1025, 16384):
         x, loc, pos = x_all[:bs], loc_all[:bs], pos_all[:bs]
         pool = torch.zeros(POOL_SLOTS_1 * 528, dtype=torch.uint8, device=DEV)
         err = _err(K)
@@ -644,14 +661,15 @@ def test_dequant_slots_fp4_pool_2m(K):
 @pytest.mark.parametrize("page_bits", [4, 8])
 @pytest.mark.parametrize("layout", [1, 2])
 def test_page_sizes_16_and_256(K, page_bits, layout):
-    """Pages of 16 and 256 tokens: store + RoPE, ratio-1 compressor (identity,
-    bit-exact), paged dequant through a permuted page table and the
-    selected-slot dequant, all against the oracle."""
+    """Pages of 16 and 256 tokens: store + RoPE (a batch of 300 rows, one CTA
+    per token, then one of 1100, the persistent kernels), ratio-1 compressor
+    (identity, bit-exact), paged dequant through a permuted page table and
+    the selected-slot dequant, all against the oracle."""
     from compress_kv_write_gb300 import synth
     P = 1 << page_bits
-    pages = 8
+    pages = max(8, 2816 // P)
     slots = pages * P
-    n = min(300, slots // 2)
+    n = 1400
     x = synth.store_rows_bf16(n, "cpu", page_bits)
     loc = synth.injective_slots(n, slots, "cpu", page_bits)
     cs = synth.rope_table(1024, "cpu")
@@ -665,8 +683,9 @@ def test_page_sizes_16_and_256(K, page_bits, layout):
     assert O.compress(layout, page_bits, 1, 0, v.numpy(), s.numpy(), cloc.numpy(), pool_o) == O.OK
     pool = torch.zeros(slots * O.bytes_per_token(layout), dtype=torch.uint8, device=DEV)
     err = _err(K)
-    K.kvq_store(layout, page_bits, K.FLAG_ROPE, x.to(DEV), loc.to(DEV), pool, slots, cos_sin=cs.to(DEV),
-                pos=pos.to(DEV), err=err)
+    for b0, b1 in ((0, 300), (300, n)):
+        K.kvq_store(layout, page_bits, K.FLAG_ROPE, x[b0:b1].to(DEV), loc[b0:b1].to(DEV), pool, slots,
+                    cos_sin=cs.to(DEV), pos=pos[b0:b1].to(DEV), err=err)
     K.kvq_compress(layout, page_bits, 1, 0, v.to(DEV), s.to(DEV), cloc.to(DEV), pool, slots, err=err)
     pt = synth.page_table_perm(pages, "cpu", page_bits)
     ws = torch.empty((slots, 512), dtype=torch.bfloat16, device=DEV)
@@ -686,16 +705,18 @@ def test_page_sizes_16_and_256(K, page_bits, layout):
 # --------------------------------------------------------------------------- decode-time compressor
 
 @pytest.mark.parametrize("layout", [1, 2])
-@pytest.mark.parametrize("r", [1, 2, 4, 128])
-def test_compress_decode_streams(K, layout, r):
+@pytest.mark.parametrize("r,wide", [(1, False), (2, False), (4, False), (128, False), (1, True), (2, True),
+                                    (4, True)])
+def test_compress_decode_streams(K, layout, r, wide):
     """Rows arrive one per call to a random subset of request slots, in random
     order (state indexed through req); every group a slot completes is
     compared with the oracle's pooling of that group's r rows.  r = 1 is the
     identity (bit-exact); the others follow the pooling tolerance (0.1% code
     budget over all completed groups: 16 to 48 request slots, so that every
-    ratio completes dozens of groups)."""
-    rng = np.random.default_rng(100 * layout + r)
-    n_state = 48 if r < 128 else 16
+    ratio completes dozens of groups).  The wide cases send all 1100 request
+    slots a row in every call (1100 CTAs, some SMs holding several)."""
+    rng = np.random.default_rng(100 * layout + r + (7 if wide else 0))
+    n_state = 1100 if wide else (48 if r < 128 else 16)
     calls = 3 * r + 2 if r < 128 else 2 * r + 3
     pool_slots = max(1024, -(-calls * n_state // 64) * 64)  # a fresh destination per row
     from compress_kv_write_gb300 import synth
@@ -709,7 +730,7 @@ def test_compress_decode_streams(K, layout, r):
     groups = []                           # (slot, first row index, dest slot, pos)
     free_slots = list(rng.permutation(pool_slots))
     for call in range(calls):
-        active = np.flatnonzero(rng.random(n_state) < (0.8 if r < 128 else 1.0))
+        active = np.flatnonzero(rng.random(n_state) < (0.8 if r < 128 and not wide else 1.0))
         if active.size == 0:
             continue
         req = rng.permutation(active).astype(np.int32)
@@ -773,9 +794,10 @@ def test_compress_decode_bad_state_index(K):
 def test_store_strided_rows(K, layout, dtype, flags):
     """x is the K slice of a wider projection: 512 columns at a 128-byte offset
     inside wider rows (x_row_stride > 512).  The pool must hold the bytes the
-    oracle writes from the contiguous copy of the same rows."""
+    oracle writes from the contiguous copy of the same rows.  1400 rows in two
+    calls: 300 (one CTA per token) and 1100 (the persistent kernels)."""
     from compress_kv_write_gb300 import synth
-    n, slots = 300, 1024
+    n, slots = 1400, 2048
     seed = 900 + layout * 10 + flags
     xc = synth.store_rows_bf16(n, "cpu", seed)
     if dtype == "f32":
@@ -795,9 +817,13 @@ def test_store_strided_rows(K, layout, dtype, flags):
                    cos_sin=cs.numpy(), pos=pos.numpy()) == O.OK
     pool = torch.zeros(slots * O.bytes_per_token(layout), dtype=torch.uint8, device=DEV)
     err = _err(K)
-    K.kvq_store(layout, 6, flags, x, loc.to(DEV), pool, slots,
-                norm_weight=w.to(DEV) if flags & 2 else None, eps=1e-6,
-                cos_sin=cs.to(DEV) if flags & 1 else None, pos=pos.to(DEV) if flags & 1 else None, err=err)
+    for b0, b1 in ((0, 300), (300, n)):
+        xb = x[b0:b1]
+        assert xb.stride(0) == 512 + 3 * pad
+        K.kvq_store(layout, 6, flags, xb, loc[b0:b1].to(DEV), pool, slots,
+                    norm_weight=w.to(DEV) if flags & 2 else None, eps=1e-6,
+                    cos_sin=cs.to(DEV) if flags & 1 else None, pos=pos[b0:b1].to(DEV) if flags & 1 else None,
+                    err=err)
     torch.cuda.synchronize()
     assert err.item() == 0
     got = np_u8(pool)
@@ -879,16 +905,22 @@ def test_kernels_reproduce_handworked_blocks(K):
     """Every hand-worked block of tests/golden, stored by the CUDA store kernels
     (fp32 input, no fused math) in quant blocks 0, 9 and 15 of its own token:
     the code and scale bytes must be the hand-derived ones, and the paged
-    dequant must give the hand-derived values."""
+    dequant must give the hand-derived values.  The batch runs alone (one
+    CTA per token) and tiled past 1024 rows (the persistent kernels; the
+    first copy is checked)."""
     from golden_io import load_blocks
-    for layout, fname in ((O.V41, "v41_blocks.txt"), (O.FP4, "fp4_blocks.txt")):
+    for layout, fname, tiled in ((O.V41, "v41_blocks.txt", False), (O.FP4, "fp4_blocks.txt", False),
+                                 (O.V41, "v41_blocks.txt", True), (O.FP4, "fp4_blocks.txt", True)):
         cases = load_blocks(fname)
         blocks = (0, 9, 15)
-        n = len(cases) * len(blocks)
-        x = np.zeros((n, 512), np.float32)
+        n1 = len(cases) * len(blocks)
+        x = np.zeros((n1, 512), np.float32)
         for ci, (_, vals, _, _, _) in enumerate(cases):
             for bi, blk in enumerate(blocks):
                 x[ci * len(blocks) + bi, blk * 32:(blk + 1) * 32] = vals
+        if tiled:
+            x = _both_paths(x)[1]
+        n = x.shape[0]
         slots = max(64, -(-n // 64) * 64)
         pool = torch.zeros(slots * O.bytes_per_token(layout), dtype=torch.uint8, device=DEV)
         loc = torch.arange(n, dtype=torch.int64, device=DEV)
@@ -901,6 +933,9 @@ def test_kernels_reproduce_handworked_blocks(K):
         assert err.item() == 0
         codes, scales = gather_rows(np_u8(pool), layout, 6, np.arange(n))
         deq = out.float().cpu().numpy()
+        if tiled:  # every copy of the batch stored alike
+            assert (codes == np.tile(codes[:n1], (n // n1, 1))).all()
+            assert (scales == np.tile(scales[:n1], (n // n1, 1))).all()
         cpb = 32 if layout == O.V41 else 16          # code bytes per quant block
         for ci, (name, _, scale, cbytes, dvals) in enumerate(cases):
             for bi, blk in enumerate(blocks):
