@@ -173,12 +173,14 @@ def _rotation(per_set_bytes, cap=64):
 
 
 def store_kernel_name(layout, flags, bs):
-    """The store kernel a batch of bs tokens runs on (layout 1 = V41): the
-    library takes one CTA per token up to 1024 tokens (512 for the plain V41
-    store), its persistent kernels beyond."""
+    """The store kernel a batch of bs tokens runs on (layout 1 = V41, flags
+    1 = RoPE, 2 = norm): the library takes one CTA per token up to 1024
+    tokens (512 for the plain V41 store), its persistent kernels beyond."""
     if bs <= (512 if (layout == 1 and flags == 0) else 1024):
         return "store_token_kernel"
-    return "store_warp_kernel" if (layout == 1 and flags != 1) else "store_half_kernel"
+    if layout == 1 and flags == 1:  # RoPE only: the half-warp kernel from 12288 tokens
+        return "store_half_kernel" if bs >= 12288 else "store_warp_kernel"
+    return "store_warp_kernel" if layout == 1 else "store_half_kernel"
 
 
 class StoreWorkload(Workload):

@@ -831,10 +831,15 @@ kvq_status launch_persistent(const StoreArgs &a, int64_t tokens_per_warp, int sk
 //    the next launch's warps become resident (and prefetch) sooner; with
 //    fewer tokens per warp the four times larger CTA count costs more in
 //    dispatch than it saves.
-//  * V41 with RoPE only: the half-warp kernel (the rotation spread over all
-//    16 lanes), one-warp CTAs, half the warps' remainder front-loaded.
+//  * V41 with RoPE only: from kRopeHalfMin tokens the half-warp kernel (the
+//    rotation spread over all 16 lanes), one-warp CTAs, half the warps'
+//    remainder front-loaded; below, one warp per token in four-warp CTAs
+//    (4096 tokens: 2.65 against 3.46 us, 8192: 4.00 against 4.60 us; equal
+//    at 12288, and 15% slower at 16384).
 //  * V41_FP4: the half-warp kernel (each block's e4m3 scale, division and
 //    reciprocal computed once), four-warp CTAs.
+constexpr int64_t kRopeHalfMin = 12288;
+
 template <Layout L, int PB, bool B16, bool L64, bool N, bool R>
 kvq_status launch_store(const StoreArgs &a, cudaStream_t stream) {
     if constexpr (L == Layout::V41 && !(R && !N)) {
@@ -862,6 +867,10 @@ kvq_status launch_store(const StoreArgs &a, cudaStream_t stream) {
         }
         return launch_persistent<kern4, 4, 4 * wsm>(a, 1, 0, stream);
     } else if constexpr (L == Layout::V41) {
+        if (a.n < kRopeHalfMin) {
+            constexpr size_t wsm = WarpStoreSmem<B16, R>::kWarpBytes;
+            return launch_persistent<store_warp_kernel<L, PB, B16, L64, N, R, 4>, 4, 4 * wsm>(a, 1, 0, stream);
+        }
         using SM = StoreSmem<L, B16, R, N>;
         return launch_persistent<store_half_kernel<L, PB, B16, L64, N, R, 1>, 1, SM::bytes(1)>(a, 2, 2, stream);
     } else {

@@ -339,6 +339,37 @@ def test_store_batch_sweep(K, sweep_inputs, flags):
         check_tolerance(O.V41, *[np.concatenate(a) for a in acc])
 
 
+@pytest.mark.parametrize("page_bits", [2, 6])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("loc64", [False, True])
+def test_v41_rope_store_both_persistent_mappings(K, page_bits, dtype, loc64):
+    """The V41 store + RoPE takes one warp per token below 12288 tokens and
+    the half-warp kernel from there: 12287 and 12289 rows, bit-exact over the
+    whole pool against the oracle."""
+    from compress_kv_write_gb300 import synth
+    slots = 1 << 14
+    cs = synth.rope_table(8192, "cpu")
+    for n in (12287, 12289):
+        seed = 70 + page_bits * 4 + int(loc64) * 2 + (dtype == "f32") + n % 3
+        x = synth.store_rows_bf16(n, "cpu", seed)
+        if dtype == "f32":
+            x = x.float() * 1.25
+        loc = synth.injective_slots(n, slots, "cpu", seed, dtype=torch.int64 if loc64 else torch.int32)
+        pos = synth.positions(n, "cpu", seed, max_pos=8192)
+        x_np = x.numpy() if dtype == "f32" else _bf16_np(x)
+        pool_o = np.zeros(slots * 528, np.uint8)
+        assert O.store(O.V41, page_bits, O.ROPE, x_np, loc.numpy(), pool_o, cos_sin=cs.numpy(),
+                       pos=pos.numpy()) == O.OK
+        pool = torch.zeros(slots * 528, dtype=torch.uint8, device=DEV)
+        err = _err(K)
+        K.kvq_store(K.V41, page_bits, K.FLAG_ROPE, x.to(DEV), loc.to(DEV), pool, slots, cos_sin=cs.to(DEV),
+                    pos=pos.to(DEV), err=err)
+        torch.cuda.synchronize()
+        assert err.item() == 0
+        got = np_u8(pool)
+        assert (got == pool_o).all(), (n, np.flatnonzero(got != pool_o)[:8])
+
+
 # --------------------------------------------------------------------------- FP4 store + dequant
 
 POOL_SLOTS_2 = 1 << 21
