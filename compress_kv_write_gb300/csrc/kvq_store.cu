@@ -175,9 +175,14 @@ __global__ void __launch_bounds__(32 * kWarps, 32 / kWarps) store_warp_kernel(co
     int cnt;
     token_range(a, gw, start, cnt);
 
-    // While the upstream grid drains: pull this warp's first NS rows and its
-    // slot / position lines into L2 (hints only; the loads come after the wait).
-    if (lane < cnt && lane < NS) prefetch_l2_bulk(a.x + (start + lane) * a.row_stride_bytes, SM::XB);
+    // While the upstream grid drains: pull this warp's first rows and its
+    // slot / position lines into L2 (hints only; the loads come after the
+    // wait).  Only the rows requested first: more compete with the upstream
+    // grid's tail (measured at 16384 tokens: norm + RoPE 6.46 us with four
+    // rows, 6.06 with its two in flight; the plain store 4.82 with four,
+    // 4.77 with one).
+    constexpr int kPrefetchRows = kRope ? D : 1;
+    if (lane < cnt && lane < kPrefetchRows) prefetch_l2_bulk(a.x + (start + lane) * a.row_stride_bytes, SM::XB);
     if (lane == 0 && cnt > 0) {
         prefetch_l2(kLoc64 ? static_cast<const void *>(static_cast<const int64_t *>(a.loc) + start)
                            : static_cast<const void *>(static_cast<const int32_t *>(a.loc) + start));
@@ -519,9 +524,14 @@ __global__ void __launch_bounds__(32 * kWarps, 16 / kWarps) store_half_kernel(co
     // 32-byte code stores need a 32-byte aligned pool (the ABI asks for 16)
     const bool pool32 = (reinterpret_cast<uintptr_t>(a.pool) & 31) == 0;
 
-    // While the upstream grid drains: L2 hints for this warp's first NS pairs
-    // and its slot / position lines (the loads come after the wait).
-    if (lane < cnt && lane < 2 * NS) prefetch_l2_bulk(a.x + (start + lane) * a.row_stride_bytes, SM::XB);
+    // While the upstream grid drains: L2 hints for this warp's first rows and
+    // its slot / position lines (the loads come after the wait).  Two pairs;
+    // one for FP4 with few tokens per warp.  More compete with the upstream
+    // grid's tail (measured at 16384 tokens: store + RoPE 5.55 us with four
+    // pairs, 5.09 with two; FP4 4.42 with four, 4.26 with two, 4.07 with one;
+    // FP4 at 32768 tokens: 8.2, 6.7 and 7.5 us).
+    const int pf_rows = (L == Layout::FP4 && a.per_warp <= 5) ? 2 : 4;
+    if (lane < cnt && lane < pf_rows) prefetch_l2_bulk(a.x + (start + lane) * a.row_stride_bytes, SM::XB);
     if (lane == 0 && cnt > 0) {
         prefetch_l2(kLoc64 ? static_cast<const void *>(static_cast<const int64_t *>(a.loc) + start)
                            : static_cast<const void *>(static_cast<const int32_t *>(a.loc) + start));
