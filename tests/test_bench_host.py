@@ -101,3 +101,32 @@ def test_source_hash_ignores_comments_only():
     c = "int f(int x) { return 3 * x; }"
     assert bench._code_only(a) == bench._code_only(b)
     assert bench._code_only(a) != bench._code_only(c)
+
+
+def _csrc_constant(fname, name):
+    import re
+    text = open(os.path.join(ROOT, "compress_kv_write_gb300", "csrc", fname)).read()
+    return int(re.search(r"constexpr int64_t " + name + r" = (\d+);", text).group(1))
+
+
+def test_store_kernel_names_follow_the_library_dispatch():
+    """bench.py names the store kernel a batch runs on (the dominant kernel of
+    a store record): its size limits are the library's dispatch constants."""
+    small = _csrc_constant("kvq_store.cuh", "kStoreSmallMax")
+    small_plain = _csrc_constant("kvq_store.cuh", "kStoreSmallMaxPlainV41")
+    rope_half = _csrc_constant("kvq_store.cu", "kRopeHalfMin")
+    name = bench.store_kernel_name
+    for layout, flags in ((1, 1), (1, 2), (1, 3), (2, 0), (2, 1), (2, 3)):
+        assert name(layout, flags, small) == "store_token_kernel"
+        assert name(layout, flags, small + 1) != "store_token_kernel"
+    assert name(1, 0, small_plain) == "store_token_kernel"
+    assert name(1, 0, small_plain + 1) == "store_warp_kernel"
+    assert name(1, 1, rope_half - 1) == "store_warp_kernel"
+    assert name(1, 1, rope_half) == "store_half_kernel"
+    assert name(1, 3, 16384) == "store_warp_kernel" and name(2, 0, 16384) == "store_half_kernel"
+
+
+def test_kernel_sources_exist():
+    for files in bench.KERNEL_SOURCES.values():
+        for fn in files:
+            assert os.path.exists(os.path.join(ROOT, "compress_kv_write_gb300", "csrc", fn)), fn
