@@ -836,11 +836,12 @@ kvq_status launch_persistent(const StoreArgs &a, int64_t tokens_per_warp, int sk
 
 // Which kernel serves which instance (each choice measured at 16384 tokens):
 //  * V41 without RoPE, and the fused norm + RoPE: one warp per token.  The
-//    norm + RoPE instance launches one-warp CTAs from three tokens per
-//    resident warp up, so that a finished warp frees its slot at once and
-//    the next launch's warps become resident (and prefetch) sooner; with
-//    fewer tokens per warp the four times larger CTA count costs more in
-//    dispatch than it saves.
+//    norm + RoPE instance launches one-warp CTAs from two and a half tokens
+//    per resident warp up, so that a finished warp frees its slot at once
+//    and the next launch's warps become resident (and prefetch) sooner
+//    (12288 tokens: 5.55 against 5.92 us); with fewer tokens per warp the
+//    four times larger CTA count costs more in dispatch than it saves (8192
+//    tokens: 6.34 against 4.52 us).
 //  * V41 with RoPE only: from kRopeHalfMin tokens the half-warp kernel (the
 //    rotation spread over all 16 lanes), one-warp CTAs, half the warps'
 //    remainder front-loaded; below, one warp per token in four-warp CTAs
@@ -862,7 +863,7 @@ kvq_status launch_store(const StoreArgs &a, cudaStream_t stream) {
             kvq_status st = resident_grid<kern1, 32>(wsm, &cap1);
             if (st == KVQ_OK) st = resident_grid<kern4, 128>(4 * wsm, &cap4);
             if (st != KVQ_OK) return st;
-            if (cap1 >= 4 * cap4 && a.n >= 3 * cap1) {
+            if (cap1 >= 4 * cap4 && 2 * a.n >= 5 * cap1) {
                 // Up to four tokens per warp, two in flight instead of three
                 // (a smaller first burst: 16384 tokens 6.61 -> 6.46 us; at 32768
                 // tokens three are faster, 10.96 against 11.96 us).
