@@ -178,9 +178,11 @@ def store_kernel_name(layout, flags, bs):
     tokens (512 for the plain V41 store), its persistent kernels beyond."""
     if bs <= (512 if (layout == 1 and flags == 0) else 1024):
         return "store_token_kernel"
-    if layout == 1 and flags == 1:  # RoPE only: the half-warp kernel from 12288 tokens
-        return "store_half_kernel" if bs >= 12288 else "store_warp_kernel"
-    return "store_warp_kernel" if layout == 1 else "store_half_kernel"
+    if layout != 1:
+        return "store_half_kernel"
+    # V41: the half-warp kernel from 12288 tokens with RoPE only, 16384 plain,
+    # 65536 with the norm; one warp per token below
+    return "store_half_kernel" if bs >= {1: 12288, 0: 16384}.get(flags, 65536) else "store_warp_kernel"
 
 
 class StoreWorkload(Workload):

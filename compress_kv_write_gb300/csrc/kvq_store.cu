@@ -834,8 +834,12 @@ kvq_status launch_persistent(const StoreArgs &a, int64_t tokens_per_warp, int sk
                            partition(a, warps, skew_div > 0 ? warps / skew_div : 0));
 }
 
-// Which kernel serves which instance (each choice measured at 16384 tokens):
-//  * V41 without RoPE, and the fused norm + RoPE: one warp per token.  The
+// Which kernel serves which instance (past the one-CTA-per-token batches):
+//  * Large V41 batches, from kPlainHalfMin tokens without the norm and from
+//    kNormHalfMin with it: the half-warp kernel in four-warp CTAs (plain:
+//    equal at 16384 tokens, 8-11% faster at 20480-32768; norm + RoPE: 4%
+//    slower at 32768, 1-3% faster at 65536-262144).
+//  * Below, V41 without RoPE, and the fused norm + RoPE: one warp per token.  The
 //    norm + RoPE instance launches one-warp CTAs from two and a half tokens
 //    per resident warp up, so that a finished warp frees its slot at once
 //    and the next launch's warps become resident (and prefetch) sooner
@@ -849,11 +853,17 @@ kvq_status launch_persistent(const StoreArgs &a, int64_t tokens_per_warp, int sk
 //    at 12288, and 15% slower at 16384).
 //  * V41_FP4: the half-warp kernel (each block's e4m3 scale, division and
 //    reciprocal computed once), four-warp CTAs.
-constexpr int64_t kRopeHalfMin = 12288;
+constexpr int64_t kRopeHalfMin = 12288;   // V41 store + RoPE
+constexpr int64_t kPlainHalfMin = 16384;  // V41 store
+constexpr int64_t kNormHalfMin = 65536;   // V41 store with the norm
 
 template <Layout L, int PB, bool B16, bool L64, bool N, bool R>
 kvq_status launch_store(const StoreArgs &a, cudaStream_t stream) {
     if constexpr (L == Layout::V41 && !(R && !N)) {
+        if (a.n >= (N ? kNormHalfMin : kPlainHalfMin)) {
+            using SMh = StoreSmem<L, B16, R, N>;
+            return launch_persistent<store_half_kernel<L, PB, B16, L64, N, R, 4>, 4, SMh::bytes(4)>(a, 2, 0, stream);
+        }
         constexpr size_t wsm = WarpStoreSmem<B16, R>::kWarpBytes;
         constexpr auto kern4 = store_warp_kernel<L, PB, B16, L64, N, R, 4>;
         if constexpr (N && R) {

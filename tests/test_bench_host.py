@@ -115,6 +115,8 @@ def test_store_kernel_names_follow_the_library_dispatch():
     small = _csrc_constant("kvq_store.cuh", "kStoreSmallMax")
     small_plain = _csrc_constant("kvq_store.cuh", "kStoreSmallMaxPlainV41")
     rope_half = _csrc_constant("kvq_store.cu", "kRopeHalfMin")
+    plain_half = _csrc_constant("kvq_store.cu", "kPlainHalfMin")
+    norm_half = _csrc_constant("kvq_store.cu", "kNormHalfMin")
     name = bench.store_kernel_name
     for layout, flags in ((1, 1), (1, 2), (1, 3), (2, 0), (2, 1), (2, 3)):
         assert name(layout, flags, small) == "store_token_kernel"
@@ -123,7 +125,11 @@ def test_store_kernel_names_follow_the_library_dispatch():
     assert name(1, 0, small_plain + 1) == "store_warp_kernel"
     assert name(1, 1, rope_half - 1) == "store_warp_kernel"
     assert name(1, 1, rope_half) == "store_half_kernel"
-    assert name(1, 3, 16384) == "store_warp_kernel" and name(2, 0, 16384) == "store_half_kernel"
+    assert name(1, 0, plain_half - 1) == "store_warp_kernel" and name(1, 0, plain_half) == "store_half_kernel"
+    for flags in (2, 3):
+        assert name(1, flags, norm_half - 1) == "store_warp_kernel"
+        assert name(1, flags, norm_half) == "store_half_kernel"
+    assert name(2, 0, 16384) == "store_half_kernel"
 
 
 def test_kernel_sources_exist():

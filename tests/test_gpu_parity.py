@@ -339,35 +339,52 @@ def test_store_batch_sweep(K, sweep_inputs, flags):
         check_tolerance(O.V41, *[np.concatenate(a) for a in acc])
 
 
-@pytest.mark.parametrize("page_bits", [2, 6])
+@pytest.mark.parametrize("flags,switch", [(1, 12288), (0, 16384), (2, 65536), (3, 65536)])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("loc64", [False, True])
-def test_v41_rope_store_both_persistent_mappings(K, page_bits, dtype, loc64):
-    """The V41 store + RoPE takes one warp per token below 12288 tokens and
-    the half-warp kernel from there: 12287 and 12289 rows, bit-exact over the
-    whole pool against the oracle."""
+def test_v41_store_both_persistent_mappings(K, flags, switch, dtype, loc64):
+    """Large V41 batches take the half-warp kernel, smaller ones one warp per
+    token; the switch sits at 12288 tokens with RoPE only, 16384 for the plain
+    store and 65536 with the norm.  One batch on each side of it (page_bits 2
+    for the first, 6 for the second): the plain and RoPE stores bit-exact over
+    the whole pool, the norm paths under the tolerance rule with both batches
+    pooled."""
     from compress_kv_write_gb300 import synth
-    slots = 1 << 14
+    slots = 1 << (2 * switch).bit_length()
     cs = synth.rope_table(8192, "cpu")
-    for n in (12287, 12289):
-        seed = 70 + page_bits * 4 + int(loc64) * 2 + (dtype == "f32") + n % 3
+    acc = [[], [], [], [], []]
+    for n, page_bits in ((switch - 1, 2), (switch + 1, 6)):
+        seed = 70 + flags * 8 + int(loc64) * 2 + (dtype == "f32") + n % 3
         x = synth.store_rows_bf16(n, "cpu", seed)
         if dtype == "f32":
             x = x.float() * 1.25
         loc = synth.injective_slots(n, slots, "cpu", seed, dtype=torch.int64 if loc64 else torch.int32)
         pos = synth.positions(n, "cpu", seed, max_pos=8192)
+        w = synth.norm_weight("cpu", seed)
         x_np = x.numpy() if dtype == "f32" else _bf16_np(x)
         pool_o = np.zeros(slots * 528, np.uint8)
-        assert O.store(O.V41, page_bits, O.ROPE, x_np, loc.numpy(), pool_o, cos_sin=cs.numpy(),
-                       pos=pos.numpy()) == O.OK
+        assert O.store(O.V41, page_bits, flags, x_np, loc.numpy(), pool_o, norm_weight=w.numpy(), eps=1e-6,
+                       cos_sin=cs.numpy(), pos=pos.numpy()) == O.OK
         pool = torch.zeros(slots * 528, dtype=torch.uint8, device=DEV)
         err = _err(K)
-        K.kvq_store(K.V41, page_bits, K.FLAG_ROPE, x.to(DEV), loc.to(DEV), pool, slots, cos_sin=cs.to(DEV),
-                    pos=pos.to(DEV), err=err)
+        K.kvq_store(K.V41, page_bits, flags, x.to(DEV), loc.to(DEV), pool, slots,
+                    norm_weight=w.to(DEV) if flags & 2 else None, eps=1e-6,
+                    cos_sin=cs.to(DEV) if flags & 1 else None, pos=pos.to(DEV) if flags & 1 else None, err=err)
         torch.cuda.synchronize()
         assert err.item() == 0
         got = np_u8(pool)
-        assert (got == pool_o).all(), (n, np.flatnonzero(got != pool_o)[:8])
+        if flags & 2 == 0:
+            assert (got == pool_o).all(), (n, np.flatnonzero(got != pool_o)[:8])
+        else:
+            g = gather_rows(got, O.V41, page_bits, loc.numpy())
+            o = gather_rows(pool_o, O.V41, page_bits, loc.numpy())
+            y = token_prequant_many(flags, x_np, w.numpy(), 1e-6, cs.numpy()[pos.numpy()])
+            for a, b in zip(acc, (g[0], g[1], o[0], o[1], y)):
+                a.append(b)
+            written = int(g[0].astype(np.int64).sum() + g[1].astype(np.int64).sum())
+            assert int(got.astype(np.int64).sum()) == written   # nothing else touched
+    if flags & 2:
+        check_tolerance(O.V41, *[np.concatenate(a) for a in acc])
 
 
 # --------------------------------------------------------------------------- FP4 store + dequant
@@ -570,6 +587,28 @@ def test_error_paths(K):
     assert err.item() == K.kvq.DEVERR_POS
     g = gather_rows(np_u8(pool), O.V41, 6, np.arange(4))
     assert (g[1][[1, 3]] == 0).all() and (g[1][[0, 2]] != 0).any()
+    # the same two checks on the FP4 layout, with the norm: bad rows flagged and skipped
+    for flags, loc_, pos_, bit in ((K.FLAG_NORM, [3, 64, -5, 7], None, K.kvq.DEVERR_SLOT),
+                                   (K.FLAG_NORM | K.FLAG_ROPE, [0, 1, 2, 3], [0, 16, 3, -1], K.kvq.DEVERR_POS)):
+        err.zero_()
+        fpool = torch.zeros(64 * 288, dtype=torch.uint8, device=DEV)
+        w = synth.norm_weight(DEV, 1)
+        K.kvq_store(K.V41_FP4, 6, flags, x, torch.tensor(loc_, device=DEV), fpool, 64, norm_weight=w, eps=1e-6,
+                    cos_sin=cs if pos_ else None,
+                    pos=torch.tensor(pos_, dtype=torch.int32, device=DEV) if pos_ else None, err=err)
+        torch.cuda.synchronize()
+        assert err.item() == bit
+        ref = np.zeros(64 * 288, np.uint8)
+        O.store(O.FP4, 6, flags, _bf16_np(x), np.array(loc_), ref, norm_weight=w.cpu().numpy(), eps=1e-6,
+                cos_sin=cs.cpu().numpy() if pos_ else None, pos=np.array(pos_, np.int32) if pos_ else None)
+        got = np_u8(fpool)
+        assert ((got != 0) == (ref != 0)).mean() > 0.99   # the same rows written (norm: within tolerance)
+        if pos_:
+            gf = gather_rows(got, O.FP4, 6, np.arange(4))
+            assert (gf[1][[1, 3]] == 0).all() and (gf[0][[1, 3]] == 0).all()
+        else:
+            gf = gather_rows(got, O.FP4, 6, np.array([3, 7]))
+            assert (gf[1][:, :16] != 0).any()
     # bad page-table entry: flagged, that page untouched
     err.zero_()
     out = torch.full((128, 512), 7.0, dtype=torch.bfloat16, device=DEV)
