@@ -837,7 +837,7 @@ kvq_status launch_persistent(const StoreArgs &a, int64_t tokens_per_warp, int sk
 // Which kernel serves which instance (past the one-CTA-per-token batches):
 //  * Large V41 batches, from kPlainHalfMin tokens without the norm and from
 //    kNormHalfMin with it: the half-warp kernel in four-warp CTAs (plain:
-//    equal at 16384 tokens, 8-11% faster at 20480-32768; norm + RoPE: 4%
+//    equal at 16384 tokens, 8-11% faster at 20480-32768; norm + RoPE: 3%
 //    slower at 32768, 1-3% faster at 65536-262144).
 //  * Below, V41 without RoPE, and the fused norm + RoPE: one warp per token.  The
 //    norm + RoPE instance launches one-warp CTAs from two and a half tokens
