@@ -526,11 +526,13 @@ __global__ void __launch_bounds__(32 * kWarps, 16 / kWarps) store_half_kernel(co
 
     // While the upstream grid drains: L2 hints for this warp's first rows and
     // its slot / position lines (the loads come after the wait).  Two pairs;
-    // one for FP4 with few tokens per warp.  More compete with the upstream
-    // grid's tail (measured at 16384 tokens: store + RoPE 5.55 us with four
-    // pairs, 5.09 with two; FP4 4.42 with four, 4.26 with two, 4.07 with one;
-    // FP4 at 32768 tokens: 8.2, 6.7 and 7.5 us).
-    const int pf_rows = (L == Layout::FP4 && a.per_warp <= 5) ? 2 : 4;
+    // one for FP4 with few tokens per warp, the whole ring with many.  More
+    // compete with the upstream grid's tail (measured at 16384 tokens: store
+    // + RoPE 5.55 us with four pairs, 5.09 with two; FP4 4.42 with four, 4.26
+    // with two, 4.07 with one; FP4 at 32768 tokens: 8.2, 6.7 and 7.5 us); in
+    // long launches (262144 tokens, 54-108 tokens per warp) four pairs gain
+    // 1-2% over two.
+    const int pf_rows = (L == Layout::FP4 && a.per_warp <= 5) ? 2 : a.per_warp >= 48 ? 2 * NS : 4;
     if (lane < cnt && lane < pf_rows) prefetch_l2_bulk(a.x + (start + lane) * a.row_stride_bytes, SM::XB);
     if (lane == 0 && cnt > 0) {
         prefetch_l2(kLoc64 ? static_cast<const void *>(static_cast<const int64_t *>(a.loc) + start)
