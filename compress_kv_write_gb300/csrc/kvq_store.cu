@@ -3,8 +3,11 @@
 // kernels of "[sglang] DeepSeek V4.1 Paged KV Cache: V41 and FP4 formats"
 // (section 1 store_row, and the store-latency table), for both layouts.
 //
-// Two kernels share the structure below and differ in how a token maps onto
-// lanes (launch_store says which instance uses which, and why):
+// Batches of up to 1024 tokens (512 for the plain V41 store) take one
+// four-warp CTA per token (kvq_store_small.cu).  Larger ones take one of two
+// persistent kernels that share the structure below and differ in how a
+// token maps onto lanes (launch_store says which instance and batch size
+// uses which, and why):
 //
 //  * store_warp_kernel: one warp per token.  Lane l owns the 16-byte chunks
 //    l, l+32, ... of the row, so every warp load / store instruction covers
@@ -27,8 +30,8 @@
 // Shared structure: persistent CTAs (as many as are resident at once); warp
 // w owns a contiguous token range computed on the host (partition) and keeps
 // its next rows in flight in a per-warp shared-memory ring filled with
-// cp.async.  Before the PDL wait each warp prefetches its first rows into
-// L2.  Slot indices and positions of 32 tokens sit one per lane, validated
+// cp.async.  Before the PDL wait each warp prefetches into L2 the rows it
+// requests first.  Slot indices and positions of 32 tokens sit one per lane, validated
 // once, and are fetched with a shuffle.  Math is fp32; the products of the
 // RMSNorm and of the rotation are rounded one by one, as in the definition.
 #include "kvq_store.cuh"
