@@ -174,9 +174,10 @@ def _rotation(per_set_bytes, cap=64):
 
 def store_kernel_name(layout, flags, bs):
     """The store kernel a batch of bs tokens runs on (layout 1 = V41, flags
-    1 = RoPE, 2 = norm): the library takes one CTA per token up to 1024
-    tokens (512 for the plain V41 store), its persistent kernels beyond."""
-    if bs <= (512 if (layout == 1 and flags == 0) else 1024):
+    1 = RoPE, 2 = norm): the library's small-batch kernel (one or two tokens
+    per CTA) up to 1024 tokens with the norm, 3072 for the V41 store + RoPE
+    and 1536 otherwise, its persistent kernels beyond."""
+    if bs <= (1024 if flags & 2 else 3072 if (layout == 1 and flags == 1) else 1536):
         return "store_token_kernel"
     if layout != 1:
         return "store_half_kernel"

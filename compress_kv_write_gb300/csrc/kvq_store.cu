@@ -3,9 +3,9 @@
 // kernels of "[sglang] DeepSeek V4.1 Paged KV Cache: V41 and FP4 formats"
 // (section 1 store_row, and the store-latency table), for both layouts.
 //
-// Batches of up to 1024 tokens (512 for the plain V41 store) take one
-// four-warp CTA per token (kvq_store_small.cu).  Larger ones take one of two
-// persistent kernels that share the structure below and differ in how a
+// Small batches (up to 1024-3072 tokens by instance) take one four-warp CTA
+// per token or per two tokens (kvq_store_small.cu).  Larger ones take one of
+// two persistent kernels that share the structure below and differ in how a
 // token maps onto lanes (launch_store says which instance and batch size
 // uses which, and why):
 //
@@ -948,8 +948,8 @@ extern "C" kvq_status kvq_store(kvq_layout layout, int page_bits, unsigned flags
     a.pool_slots = pool_slots;
     a.err = err;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (n <= store_small_max(layout, norm, rope))
-        return launch_store_small(layout, page_bits, x_dtype == KVQ_BF16, loc_dtype == KVQ_I64, norm, rope, a, s);
+    if (const int tpc = store_small_tokens_per_cta(layout, norm, rope, n))
+        return launch_store_small(layout, page_bits, x_dtype == KVQ_BF16, loc_dtype == KVQ_I64, norm, rope, tpc, a, s);
     return with_layout(layout, [&](auto Lc) {
         return with_page_bits(page_bits, [&](auto PBc) {
             return with_bool(x_dtype == KVQ_BF16, [&](auto B16) {

@@ -29,19 +29,28 @@ struct StoreArgs {
     int64_t warps;
 };
 
-// Batches up to this many tokens take one four-warp CTA per token
-// (kvq_store_small.cu), larger ones the persistent kernels: measured at 512,
-// 1024 and 2048 tokens, the CTA per token wins up to 1024 with RoPE or the
-// norm and for V41_FP4, and ties at 512 for the plain V41 store.
-constexpr int64_t kStoreSmallMax = 1024;
-constexpr int64_t kStoreSmallMaxPlainV41 = 512;
-inline int64_t store_small_max(int layout, bool norm, bool rope) {
-    return (layout == KVQ_LAYOUT_V41 && !norm && !rope) ? kStoreSmallMaxPlainV41 : kStoreSmallMax;
+// Small batches take the small-batch kernel (kvq_store_small.cu): one
+// four-warp CTA per token, or per two tokens in the middle range, where one
+// CTA per token costs more to schedule and one warp per token has the longer
+// chain.  Larger ones take the persistent kernels.  Measured from 64 to 4096
+// tokens; the limits are the last sizes at which each form wins:
+constexpr int64_t kSmallNormMax = 1024;     // with the norm: one token per CTA up to here
+constexpr int64_t kSmallRopeOneMax = 512;   // V41 store + RoPE: one token per CTA ...
+constexpr int64_t kSmallRopeTwoMax = 3072;  // ... then two, up to here
+constexpr int64_t kSmallOneMax = 256;       // plain V41 and V41_FP4 without the norm: one ...
+constexpr int64_t kSmallTwoMax = 1536;      // ... then two, up to here
+// Tokens per CTA of the small-batch kernel for a batch of n tokens (0: the
+// persistent kernels).
+inline int store_small_tokens_per_cta(int layout, bool norm, bool rope, int64_t n) {
+    if (norm) return n <= kSmallNormMax ? 1 : 0;
+    if (layout == KVQ_LAYOUT_V41 && rope) return n <= kSmallRopeOneMax ? 1 : n <= kSmallRopeTwoMax ? 2 : 0;
+    return n <= kSmallOneMax ? 1 : n <= kSmallTwoMax ? 2 : 0;
 }
 
-// One CTA per token: layout, page_bits, input dtype, index dtype and flags
-// as validated by kvq_store.
+// One four-warp CTA per token (tokens_per_cta 1) or per two tokens (2):
+// layout, page_bits, input dtype, index dtype and flags as validated by
+// kvq_store.
 kvq_status launch_store_small(int layout, int page_bits, bool bf16, bool loc64, bool norm, bool rope,
-                              const StoreArgs &a, cudaStream_t stream);
+                              int tokens_per_cta, const StoreArgs &a, cudaStream_t stream);
 
 }  // namespace kvq

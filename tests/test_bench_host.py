@@ -112,17 +112,17 @@ def _csrc_constant(fname, name):
 def test_store_kernel_names_follow_the_library_dispatch():
     """bench.py names the store kernel a batch runs on (the dominant kernel of
     a store record): its size limits are the library's dispatch constants."""
-    small = _csrc_constant("kvq_store.cuh", "kStoreSmallMax")
-    small_plain = _csrc_constant("kvq_store.cuh", "kStoreSmallMaxPlainV41")
+    small_norm = _csrc_constant("kvq_store.cuh", "kSmallNormMax")
+    small_rope = _csrc_constant("kvq_store.cuh", "kSmallRopeTwoMax")
+    small = _csrc_constant("kvq_store.cuh", "kSmallTwoMax")
     rope_half = _csrc_constant("kvq_store.cu", "kRopeHalfMin")
     plain_half = _csrc_constant("kvq_store.cu", "kPlainHalfMin")
     norm_half = _csrc_constant("kvq_store.cu", "kNormHalfMin")
     name = bench.store_kernel_name
-    for layout, flags in ((1, 1), (1, 2), (1, 3), (2, 0), (2, 1), (2, 3)):
-        assert name(layout, flags, small) == "store_token_kernel"
-        assert name(layout, flags, small + 1) != "store_token_kernel"
-    assert name(1, 0, small_plain) == "store_token_kernel"
-    assert name(1, 0, small_plain + 1) == "store_warp_kernel"
+    for layout, flags, limit in ((1, 0, small), (1, 1, small_rope), (1, 2, small_norm), (1, 3, small_norm),
+                                 (2, 0, small), (2, 1, small), (2, 3, small_norm)):
+        assert name(layout, flags, limit) == "store_token_kernel"
+        assert name(layout, flags, limit + 1) != "store_token_kernel"
     assert name(1, 1, rope_half - 1) == "store_warp_kernel"
     assert name(1, 1, rope_half) == "store_half_kernel"
     assert name(1, 0, plain_half - 1) == "store_warp_kernel" and name(1, 0, plain_half) == "store_half_kernel"

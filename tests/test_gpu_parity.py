@@ -85,16 +85,17 @@ def test_fp32_store_and_dequant_64_tokens(K):
 @pytest.mark.parametrize("loc64", [False, True])
 @pytest.mark.parametrize("flags", [0, 1, 2, 3])
 def test_store_instances_ragged(K, page_bits, layout, dtype, loc64, flags):
-    """Every store instance on ragged batches: 1, 37 and 301 rows (batches of
-    up to 1024 tokens take one CTA per token) and 1537 rows (the persistent
-    kernels).  The plain and RoPE paths bit-exact over the whole pool; the
-    norm paths under the tolerance rule, the four batches pooled into one
+    """Every store instance on ragged batches of 1, 37, 301, 1537 and 3100
+    rows, which cover every store mapping: one CTA per token, two tokens per
+    CTA (301 rows plain and FP4, 1537 with RoPE only) and the persistent
+    kernels.  The plain and RoPE paths bit-exact over the whole pool; the
+    norm paths under the tolerance rule, the batches pooled into one
     comparison."""
     from compress_kv_write_gb300 import synth
-    slots = 2048
+    slots = 4096
     rng_seed = page_bits * 1000 + layout * 100 + flags * 10 + int(loc64)
     acc = [[], [], [], [], []]
-    for n in (1, 37, 301, 1537):
+    for n in (1, 37, 301, 1537, 3100):
         x = synth.store_rows_bf16(n, "cpu", rng_seed + n)
         if dtype == "f32":
             x = x.float() * 1.25          # not bf16-representable in general
@@ -132,10 +133,12 @@ def test_store_instances_ragged(K, page_bits, layout, dtype, loc64, flags):
 
 # --------------------------------------------------------------------------- codecs
 
-def _both_paths(x):
-    """x (up to 1024 rows: one CTA per token) and x tiled past 1024 rows (the
-    persistent kernels), so that a codec pin covers both store mappings."""
-    return [x, np.tile(x, (-(-1025 // x.shape[0]), 1))]
+def _all_mappings(x):
+    """x itself (a small batch: one CTA per token), x tiled to 600 rows or
+    more (two tokens per CTA for the plain and FP4 stores) and x tiled past
+    3072 rows (the persistent kernels), so that a codec pin covers every store
+    mapping."""
+    return [x, np.tile(x, (-(-600 // x.shape[0]), 1)), np.tile(x, (-(-3073 // x.shape[0]), 1))]
 
 
 def test_codec_every_bf16_pattern(K):
@@ -148,7 +151,7 @@ def test_codec_every_bf16_pattern(K):
     pat = pat[rng.permutation(pat.size)]
     pad = (-pat.size) % 512
     pat1 = np.concatenate([pat, np.zeros(pad, np.uint16)]).reshape(-1, 512)
-    for pat in _both_paths(pat1):
+    for pat in _all_mappings(pat1):
         n = pat.shape[0]
         slots = -(-n // 64) * 64
         x = torch.from_numpy(pat.view(np.int16)).view(torch.bfloat16).to(DEV)
@@ -183,7 +186,7 @@ def test_codec_e4m3_midpoints(K):
     grid = np.unique(O.e4m3_decode(codes))
     x = _midpoint_rows(448.0, grid)          # byte 127: multiplier 1
     x = np.concatenate([x, _midpoint_rows(511.0, np.array([448.0, 460.0, 464.0, 480.0, 500.0]))])
-    for x in _both_paths(x):
+    for x in _all_mappings(x):
         rows_o = _oracle_store_rows(O.V41, 0, x)
         n = x.shape[0]
         pool = torch.zeros(-(-n // 64) * 64 * 528, dtype=torch.uint8, device=DEV)
@@ -200,7 +203,7 @@ def test_codec_e2m1_midpoints(K):
     x = _midpoint_rows(6.0, grid)            # scale 1.0
     x = np.concatenate([x, _midpoint_rows(6.0, np.array([5.9, 6.0, 6.2, 7.0, 100.0]))])
     x = np.clip(x, -6, 6)                    # keep the block amax at 6
-    for x in _both_paths(x):
+    for x in _all_mappings(x):
         rows_o = _oracle_store_rows(O.FP4, 0, x)
         n = x.shape[0]
         slots = -(-n // 64) * 64
@@ -219,8 +222,8 @@ def test_fp4_every_scale_byte(K):
     scale (both signs).  The stored code and scale bytes, and the dequant,
     must equal the oracle's, so every entry of the kernel's reciprocal table
     and every scale its quotient can produce is exercised.  The 8 rows run
-    alone (one CTA per token) and tiled to 1032 rows (the persistent kernel
-    with its reciprocal table)."""
+    alone (one CTA per token), tiled to 520 rows (two tokens per CTA) and to
+    3080 rows (the persistent kernel with its reciprocal table)."""
     codes = np.arange(1, 127, dtype=np.uint8)
     S = O.e4m3_decode(codes)
     amax = (S * 6).astype(np.float32)
@@ -237,7 +240,7 @@ def test_fp4_every_scale_byte(K):
     nb = -(-len(rows) // 16) * 16
     rows += [np.zeros(32, np.float32)] * (nb - len(rows))
     x1 = np.stack(rows).reshape(-1, 512)
-    for dtype, reps in (("f32", 1), ("bf16", 1), ("f32", 129), ("bf16", 129)):
+    for dtype, reps in (("f32", 1), ("bf16", 1), ("f32", 65), ("bf16", 65), ("f32", 385), ("bf16", 385)):
         x = np.tile(x1, (reps, 1))
         xx = x if dtype == "f32" else O.bf16_bits(x).reshape(x.shape)
         rows_o = _oracle_store_rows(O.FP4, 0, xx)
@@ -309,8 +312,8 @@ def sweep_inputs():
 def test_store_batch_sweep(K, sweep_inputs, flags):
     """bf16 rows with outliers, pool of 2^20 slots: store, store + RoPE and
     fused K RMSNorm + RoPE at every batch size of the sweep (1, 8, 64, 512,
-    16384) and on both sides of the one-CTA-per-token limit (1024, 1025),
-    each into a fresh pool.  Plain and RoPE stores are bit-exact; the fused
+    16384) and at 1024 and 1025 tokens (the small-batch kernel's limit with
+    the norm), each into a fresh pool.  Plain and RoPE stores are bit-exact; the fused
     norm path follows the tolerance rule with the batches pooled into one
     comparison."""
     x_all, loc_all, pos_all, cs, w = sweep_inputs
@@ -731,15 +734,16 @@ def test_dequant_slots_fp4_pool_2m(K):
 @pytest.mark.parametrize("page_bits", [4, 8])
 @pytest.mark.parametrize("layout", [1, 2])
 def test_page_sizes_16_and_256(K, page_bits, layout):
-    """Pages of 16 and 256 tokens: store + RoPE (a batch of 300 rows, one CTA
-    per token, then one of 1100, the persistent kernels), ratio-1 compressor
-    (identity, bit-exact), paged dequant through a permuted page table and
-    the selected-slot dequant, all against the oracle."""
+    """Pages of 16 and 256 tokens: store + RoPE (batches of 300, 1100 and 3200
+    rows: one CTA per token, two tokens per CTA, the persistent kernels),
+    ratio-1 compressor (identity, bit-exact), paged dequant through a
+    permuted page table and the selected-slot dequant, all against the
+    oracle."""
     from compress_kv_write_gb300 import synth
     P = 1 << page_bits
-    pages = max(8, 2816 // P)
+    pages = max(8, 9216 // P)
     slots = pages * P
-    n = 1400
+    n = 4600
     x = synth.store_rows_bf16(n, "cpu", page_bits)
     loc = synth.injective_slots(n, slots, "cpu", page_bits)
     cs = synth.rope_table(1024, "cpu")
@@ -753,7 +757,7 @@ def test_page_sizes_16_and_256(K, page_bits, layout):
     assert O.compress(layout, page_bits, 1, 0, v.numpy(), s.numpy(), cloc.numpy(), pool_o) == O.OK
     pool = torch.zeros(slots * O.bytes_per_token(layout), dtype=torch.uint8, device=DEV)
     err = _err(K)
-    for b0, b1 in ((0, 300), (300, n)):
+    for b0, b1 in ((0, 300), (300, 1400), (1400, n)):
         K.kvq_store(layout, page_bits, K.FLAG_ROPE, x[b0:b1].to(DEV), loc[b0:b1].to(DEV), pool, slots,
                     cos_sin=cs.to(DEV), pos=pos[b0:b1].to(DEV), err=err)
     K.kvq_compress(layout, page_bits, 1, 0, v.to(DEV), s.to(DEV), cloc.to(DEV), pool, slots, err=err)
@@ -864,10 +868,10 @@ def test_compress_decode_bad_state_index(K):
 def test_store_strided_rows(K, layout, dtype, flags):
     """x is the K slice of a wider projection: 512 columns at a 128-byte offset
     inside wider rows (x_row_stride > 512).  The pool must hold the bytes the
-    oracle writes from the contiguous copy of the same rows.  1400 rows in two
-    calls: 300 (one CTA per token) and 1100 (the persistent kernels)."""
+    oracle writes from the contiguous copy of the same rows.  3500 rows in
+    three calls of 100, 300 and 3100 rows: every store mapping."""
     from compress_kv_write_gb300 import synth
-    n, slots = 1400, 2048
+    n, slots = 3500, 4096
     seed = 900 + layout * 10 + flags
     xc = synth.store_rows_bf16(n, "cpu", seed)
     if dtype == "f32":
@@ -887,7 +891,7 @@ def test_store_strided_rows(K, layout, dtype, flags):
                    cos_sin=cs.numpy(), pos=pos.numpy()) == O.OK
     pool = torch.zeros(slots * O.bytes_per_token(layout), dtype=torch.uint8, device=DEV)
     err = _err(K)
-    for b0, b1 in ((0, 300), (300, n)):
+    for b0, b1 in ((0, 100), (100, 400), (400, n)):
         xb = x[b0:b1]
         assert xb.stride(0) == 512 + 3 * pad
         K.kvq_store(layout, 6, flags, xb, loc[b0:b1].to(DEV), pool, slots,
@@ -976,11 +980,12 @@ def test_kernels_reproduce_handworked_blocks(K):
     (fp32 input, no fused math) in quant blocks 0, 9 and 15 of its own token:
     the code and scale bytes must be the hand-derived ones, and the paged
     dequant must give the hand-derived values.  The batch runs alone (one
-    CTA per token) and tiled past 1024 rows (the persistent kernels; the
-    first copy is checked)."""
+    CTA per token) and tiled into every other store mapping (two tokens per
+    CTA, the persistent kernels; the first copy is checked)."""
     from golden_io import load_blocks
-    for layout, fname, tiled in ((O.V41, "v41_blocks.txt", False), (O.FP4, "fp4_blocks.txt", False),
-                                 (O.V41, "v41_blocks.txt", True), (O.FP4, "fp4_blocks.txt", True)):
+    for layout, fname, tiled in ((O.V41, "v41_blocks.txt", 0), (O.FP4, "fp4_blocks.txt", 0),
+                                 (O.V41, "v41_blocks.txt", 1), (O.FP4, "fp4_blocks.txt", 1),
+                                 (O.V41, "v41_blocks.txt", 2), (O.FP4, "fp4_blocks.txt", 2)):
         cases = load_blocks(fname)
         blocks = (0, 9, 15)
         n1 = len(cases) * len(blocks)
@@ -988,8 +993,7 @@ def test_kernels_reproduce_handworked_blocks(K):
         for ci, (_, vals, _, _, _) in enumerate(cases):
             for bi, blk in enumerate(blocks):
                 x[ci * len(blocks) + bi, blk * 32:(blk + 1) * 32] = vals
-        if tiled:
-            x = _both_paths(x)[1]
+        x = _all_mappings(x)[tiled]
         n = x.shape[0]
         slots = max(64, -(-n // 64) * 64)
         pool = torch.zeros(slots * O.bytes_per_token(layout), dtype=torch.uint8, device=DEV)
