@@ -390,6 +390,48 @@ def test_v41_store_both_persistent_mappings(K, flags, switch, dtype, loc64):
         check_tolerance(O.V41, *[np.concatenate(a) for a in acc])
 
 
+@pytest.mark.parametrize("layout", [1, 2])
+@pytest.mark.parametrize("flags", [0, 1, 3])
+def test_store_random_batch_sizes(K, layout, flags):
+    """Seeded log-uniform batch sizes from 1 to 40000 tokens (and the sizes
+    on each side of every switch between the store mappings), bf16 rows,
+    int32 or int64 slots: the plain and RoPE paths bit-exact over the whole
+    pool, the norm path under the tolerance rule with all batches pooled."""
+    from compress_kv_write_gb300 import synth
+    rng = np.random.default_rng(300 + 10 * layout + flags)
+    sizes = sorted(set(int(v) for v in np.exp(rng.uniform(0, np.log(40000), 6))) |
+                   {256, 257, 512, 513, 1536, 1537, 3072, 3073, 12287, 12288, 16383, 16384})
+    slots = 1 << 17
+    cs = synth.rope_table(8192, "cpu")
+    acc = [[], [], [], [], []]
+    for n in sizes:
+        seed = 500 + n
+        x = synth.store_rows_bf16(n, "cpu", seed)
+        loc = synth.injective_slots(n, slots, "cpu", seed, dtype=torch.int64 if n % 2 else torch.int32)
+        pos = synth.positions(n, "cpu", seed, max_pos=8192)
+        w = synth.norm_weight("cpu", seed)
+        x_np = _bf16_np(x)
+        rows_o = _oracle_store_rows(layout, flags, x_np, w.numpy(), 1e-6, cs.numpy(), pos.numpy())
+        pool = torch.zeros(slots * O.bytes_per_token(layout), dtype=torch.uint8, device=DEV)
+        err = _err(K)
+        K.kvq_store(layout, 6, flags, x.to(DEV), loc.to(DEV), pool, slots,
+                    norm_weight=w.to(DEV) if flags & 2 else None, eps=1e-6,
+                    cos_sin=cs.to(DEV) if flags & 1 else None, pos=pos.to(DEV) if flags & 1 else None, err=err)
+        torch.cuda.synchronize()
+        assert err.item() == 0, n
+        g = gather_rows_torch(pool, layout, 6, loc.numpy())
+        if flags & 2:
+            y = token_prequant_many(flags, x_np, w.numpy(), 1e-6, cs.numpy()[pos.numpy()])
+            for a, b in zip(acc, (g[0], g[1], rows_o[0], rows_o[1], y)):
+                a.append(b)
+        else:
+            assert (g[0] == rows_o[0]).all() and (g[1] == rows_o[1]).all(), n
+        written = int(g[0].astype(np.int64).sum() + g[1].astype(np.int64).sum())
+        assert int(pool.sum(dtype=torch.int64).item()) == written, n   # nothing else touched
+    if flags & 2:
+        check_tolerance(layout, *[np.concatenate(a) for a in acc])
+
+
 # --------------------------------------------------------------------------- FP4 store + dequant
 
 POOL_SLOTS_2 = 1 << 21
