@@ -8,10 +8,12 @@
 // the block absmax and the conversions.  The persistent kernels give a token
 // to one warp (16 values per lane), so at a few hundred tokens the launch
 // lasts as long as one warp's instruction stream.  Here a token is one CTA
-// of four warps and thread t owns the dims 4t .. 4t+3: a quarter of the
-// per-thread chain, with the norm's sum reduced over the four warps through
-// shared memory.  Semantics, roundings and error bits are those of the
-// persistent kernels (kvq_store.cu).
+// of four warps, thread t owning dims 4t .. 4t+3 (a quarter of the
+// per-thread chain), or half a CTA, eight dims per thread, where one CTA per
+// token would cost more to schedule than the shorter chain saves.  The
+// norm's sum is reduced over the token's warps through shared memory.
+// Semantics, roundings and error bits are those of the persistent kernels
+// (kvq_store.cu).
 #include "kvq_store.cuh"
 
 namespace kvq {
